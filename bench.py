@@ -1,0 +1,390 @@
+#!/usr/bin/env python
+"""Benchmark of SnapKV prefill-time KV-cache compression on GB300.
+
+One step = the whole compression (scores, pooling, selection, emission) of
+every layer of the workload, each layer with its own K/V, through the C ABI
+(snapkv_compress) on device-resident inputs.  The metric is prompt tokens
+compressed per second per layer, all heads: (prompt tokens x layers) / time.
+
+Default workload: a Llama-3-8B-shaped model at a 131072-token prompt, 32
+layers (32 query / 8 KV heads, d = 128, bf16, W = 64, avg pooling k = 13,
+C = 4096).  Each layer's K and V (537 MB) are far larger than L2, so no L2
+flush is needed between iterations.
+
+Also reported: the score kernel alone against the HBM roofline (CUDA events
+on the launching stream), the end-to-end figure through the host-buffer entry
+point (host->device copies of the inputs and device->host copies of the
+compressed cache inside the timed region), the oracle timed on host cores on
+a bounded sample, SM clocks and throttle reasons sampled during the timed
+region, and the number of library kernels launched in it.
+
+`--impl reference` times the CPU oracle instead, on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prompt tokens compressed/s per layer (all heads) and % of HBM roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="4", help="workload name (see synth.CONFIGS)")
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- peaks ---
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks ---
+
+class ClockSampler:
+    """SM clock and clock-event reasons sampled during a region (NVML)."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x20: "sync_boost", 0x40: "sw_thermal_slowdown",
+               0x80: "hw_thermal_slowdown", 0x100: "hw_power_brake_slowdown",
+               0x200: "display_clock_setting"}
+
+    def __init__(self, cuda_index: int, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []
+        self.reasons = 0
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._th = None
+        self._nvml = None
+        self._h = None
+        try:
+            import torch
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit")
+            h = ctypes.c_void_p()
+            uuid = str(torch.cuda.get_device_properties(cuda_index).uuid)
+            if nv.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(h)) != 0:
+                    raise RuntimeError("nvml handle")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nvml, self._h = nv, h
+        except Exception:
+            self._nvml = None
+
+    def _loop(self):
+        nv, h = self._nvml, self._h
+        mhz = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0:
+                self.samples.append(mhz.value)
+            if nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(self.period)
+
+    def start(self):
+        if self._nvml is not None:
+            self._th = threading.Thread(target=self._loop, daemon=True)
+            self._th.start()
+
+    def stop(self):
+        if self._th is not None:
+            self._stop.set()
+            self._th.join()
+
+    def summary(self):
+        if self._nvml is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        reasons = [n for bit, n in self.REASONS.items() if self.reasons & bit]
+        return {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------ workloads ---
+
+def workload_bytes(cfg, seqlens, esz):
+    """Algorithmic bytes of one layer: (score kernel, whole compression)."""
+    H_q, H_kv, d, W, C = cfg["H_q"], cfg["H_kv"], cfg["d"], cfg["W"], cfg["C"]
+    score = sum(L * H_kv * d * esz + W * H_q * d * esz for L in seqlens)
+    gather = sum(4 * min(C, L) * H_kv * d * esz + 4 * min(C, L) * H_kv for L in seqlens)
+    return score, score + gather
+
+
+def cpu_baseline(name, layers_total, nthreads=None, lay=None):
+    """Oracle on one full layer (all KV heads): a bounded sample."""
+    import oracle
+    import synth
+
+    cfg = synth.CONFIGS[name]
+    lay = lay if lay is not None else synth.make_layer(name, 0)
+    units = lay.B * lay.H_kv
+    nthreads = nthreads or max(1, min(units, os.cpu_count() or 1))
+    t0 = time.perf_counter()
+    oracle.compress(lay.q_win, lay.k, lay.v, lay.seqlens, lay.W, cfg["k_pool"], cfg["pool"],
+                    cfg["C"], nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    tokens = int(sum(lay.seqlens))
+    return {"value": tokens / dt, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": f"layer 0 of {layers_total}, all {lay.H_kv} KV heads, "
+                      f"{tokens} prompt tokens, fp64 C oracle, {dt:.2f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import synth
+
+    name = args.workload
+    cfg = synth.CONFIGS[name]
+    layers = args.layers or cfg["layers"]
+    lay = synth.make_layer(name, 0)
+    for _ in range(args.warmup):
+        cpu_baseline(name, layers, lay=lay)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(name, layers, lay=lay))
+    wall = time.perf_counter() - t0
+    v = statistics.median(x["value"] for x in vals)
+    seqlens = synth.config_seqlens(name)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{name}: {cfg['desc']}", "seqlens": seqlens if len(seqlens) <= 16
+                   else len(seqlens), "layers": layers,
+                   "step": "oracle on a bounded sample: one full layer, all KV heads"},
+        "cpu_baseline": {"kind": "oracle", "cores": vals[0]["cores"],
+                         "sample": vals[0]["sample"], "value": v, "unit": UNIT},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    from synth.device import make_layer_device
+    from prefill_kv_cache_gb300 import snapkv as S
+
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = f"cuda:{local_rank}"
+    S.load()
+
+    name = args.workload
+    cfg = synth.CONFIGS[name]
+    layers = args.layers or cfg["layers"]
+    W, C, kp, pool = cfg["W"], cfg["C"], cfg["k_pool"], cfg["pool"]
+    esz = 2 if cfg["dtype"] == "bf16" else 4
+
+    data = []
+    for l in range(layers):
+        q, k, v, seqlens = make_layer_device(name, l + 1000 * rank, dev)
+        data.append((q, k, v))
+    B = len(seqlens)
+    H_q, H_kv, d = cfg["H_q"], cfg["H_kv"], cfg["d"]
+    dt = data[0][1].dtype
+    outs = [(torch.empty((B, C, H_kv, d), dtype=dt, device=dev),
+             torch.empty((B, C, H_kv, d), dtype=dt, device=dev),
+             torch.empty((B, H_kv, C), dtype=torch.int32, device=dev)) for _ in range(layers)]
+    shape = S.make_shape(B, H_q, H_kv, d, dt)
+    ws = torch.empty(S.workspace_size(shape, seqlens, W, C), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    lib = S.load()
+    sl_arr = (ctypes.c_int32 * B)(*seqlens)
+    pool_code = S.pool_code(pool)
+    sh_ref = ctypes.byref(shape)
+    ws_ptr, ws_len = ws.data_ptr(), ws.numel()
+    st = stream.cuda_stream
+    calls = [(q.data_ptr(), k.data_ptr(), v.data_ptr(), ok.data_ptr(), ov.data_ptr(), oi.data_ptr())
+             for (q, k, v), (ok, ov, oi) in zip(data, outs)]
+
+    def step():
+        for qp, kp_, vp, okp, ovp, oip in calls:
+            rc = lib.snapkv_compress(sh_ref, qp, kp_, vp, sl_arr, W, kp, pool_code, C, okp, ovp,
+                                     oip, ws_ptr, ws_len, st)
+            if rc:
+                raise S.SnapKVError(rc, "snapkv_compress")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert S.get_status(ws) == S.OK
+
+    sampler = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = S.kernel_launches()
+    sampler.start()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.stop()
+    launches = S.kernel_launches() - n0
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens_per_step = sum(seqlens) * layers
+    value = tokens_per_step * world / (ms / 1e3)
+
+    # score kernel alone, per launch, on the launching stream
+    score_ms = []
+    for _ in range(2):
+        for (q, k, _), _o in zip(data, outs):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            rc = lib.snapkv_score(sh_ref, q.data_ptr(), k.data_ptr(), sl_arr, W, C, ws_ptr,
+                                  ws_len, st)
+            b.record(stream)
+            if rc:
+                raise S.SnapKVError(rc, "snapkv_score")
+            score_ms.append((a, b))
+    torch.cuda.synchronize()
+    score_avg_ms = statistics.mean(a.elapsed_time(b) for a, b in score_ms[len(data):])
+    score_bytes, compress_bytes = workload_bytes(cfg, seqlens, esz)
+    peak, peak_kind = hbm_peak()
+    achieved = score_bytes / (score_avg_ms / 1e3) / 1e9
+    compress_gbs = compress_bytes / (ms / layers / 1e3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "score_kernel_traffic.json")
+    if os.path.exists(tpath):
+        try:
+            with open(tpath) as f:
+                tinfo = json.load(f)
+            if tinfo.get("workload") == name and tinfo.get("kernel_version") == S.load().snapkv_version():
+                traffic = tinfo.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(S, torch, data, seqlens, cfg, shape, dev, stream, args, layers)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(name, layers)
+
+    if rank == 0:
+        clk = sampler.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": cfg["dtype"], "data": "synthetic",
+            "config": {
+                "workload": f"{name}: {cfg['desc']}",
+                "seqlens": seqlens if len(seqlens) <= 16 else len(seqlens),
+                "layers": layers, "us_per_layer": 1e3 * ms / layers,
+                "l2": "inputs larger than L2 (each layer's K and V: "
+                      f"{2 * sum(seqlens) * H_kv * d * esz / 1e6:.0f} MB)",
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            },
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "score (snapkv_score)", "peak_kind": peak_kind,
+                         "us_per_launch": 1e3 * score_avg_ms,
+                         "bytes_per_launch": score_bytes},
+            "roofline_compress": {"achieved": compress_gbs, "peak": peak, "unit": "GB/s",
+                                  "frac": compress_gbs / peak, "bytes_per_layer": compress_bytes},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(S, torch, data, seqlens, cfg, shape, dev, stream, args, layers):
+    """Same metric through snapkv_compress_host: pinned host in, pinned host out."""
+    W, C, kp, pool = cfg["W"], cfg["C"], cfg["k_pool"], cfg["pool"]
+    B = len(seqlens)
+    H_kv, d = cfg["H_kv"], cfg["d"]
+    dt = data[0][1].dtype
+    host = []
+    for layer in data:
+        hl = []
+        for x in layer:
+            h = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+            h.copy_(x)
+            hl.append(h)
+        host.append(tuple(hl))
+    outs = [(torch.empty((B, C, H_kv, d), dtype=dt).pin_memory(),
+             torch.empty((B, C, H_kv, d), dtype=dt).pin_memory(),
+             torch.empty((B, H_kv, C), dtype=torch.int32).pin_memory()) for _ in range(layers)]
+    staging = torch.empty(S.host_staging_size(shape, seqlens, W, C), dtype=torch.uint8,
+                          device=dev)
+
+    def step():
+        for (q, k, v), (ok, ov, oi) in zip(host, outs):
+            S.compress_host(q, k, v, seqlens, W, kp, pool, C, ok, ov, oi, staging, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    sec = (time.perf_counter() - t0) / args.steps
+    h2d = sum(sum(x.numel() * x.element_size() for x in layer) for layer in host)
+    d2h = sum(sum(x.numel() * x.element_size() for x in o) for o in outs)
+    return {"value": sum(seqlens) * layers / sec, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * sec}
+
+
+if __name__ == "__main__":
+    main()

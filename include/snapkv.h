@@ -1,0 +1,192 @@
+/*
+ * snapkv.h - C ABI of the GB300 (sm_103a) SnapKV prefill-time KV-cache
+ * compression library (libsnapkv.so).
+ *
+ * What the library computes, for each sequence b (prompt length L) and each
+ * KV head h, with W the observation window and C the total budget:
+ *
+ *   - the last W prompt queries (the observation window) attend over the
+ *     prompt keys with softmax(q.k / sqrt(d)) under the causal mask
+ *     (jisaku.com glossary "SnapKV", section "SnapKVの仕組み": Observation
+ *     Window and the algorithm flow, steps 1-2);
+ *   - each prefix key j < P = L - W gets the sum of its probabilities over
+ *     the window rows, averaged over the g = H_q / H_kv query heads of the KV
+ *     group (hotpaper.ai summary of "SnapKV: LLM Knows What You are Looking
+ *     for Before Generation": abstract and "핵심 아이디어", per-head selection;
+ *     the glossary's FAQ Q1 on MHA and GQA models);
+ *   - the scores are pooled (stride 1, kernel_size // 2 zeros of padding,
+ *     average divides by kernel_size, or maximum) (glossary, "Pooling for
+ *     Robustness"; summary, "기술적 접근법": max or average pooling, kernel
+ *     5-13);
+ *   - the C - W best prefix positions are kept, ties to the lower position
+ *     (glossary, algorithm flow step 3: keep the top-B pairs; summary,
+ *     "기술적 접근법": compressed size 1024-4096);
+ *   - the compressed cache holds the kept rows in ascending position, then
+ *     the W window rows, plus their positions (glossary, step 4: decode uses
+ *     the compressed cache).  When L <= C every position is kept.
+ *
+ * The parameter names of the glossary's usage example map as follows:
+ * window_size -> W, max_capacity_prompt -> C, kernel_size -> kernel_size,
+ * pooling ("avgpool" / "maxpool") -> pool_type.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are plain CUDA device addresses of the current device;
+ *     host pointers are ordinary process memory.  The library keeps no
+ *     pointer after a call returns and allocates no memory: the caller owns
+ *     every buffer, including the workspace.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  snapkv_compress is asynchronous on that stream and never
+ *     synchronizes.  Calls that share one workspace must not overlap in time.
+ *   - Return values are snapkv_status codes.  An argument error returns
+ *     before anything is enqueued.
+ */
+#ifndef SNAPKV_H
+#define SNAPKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SNAPKV_OK = 0,
+    SNAPKV_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned buffer */
+    SNAPKV_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels cover */
+    SNAPKV_ERR_WORKSPACE = 3,   /* workspace smaller than snapkv_workspace_size */
+    SNAPKV_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+    SNAPKV_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up */
+} snapkv_status;
+
+typedef enum { SNAPKV_POOL_AVG = 0, SNAPKV_POOL_MAX = 1 } snapkv_pool;
+
+typedef enum { SNAPKV_BF16 = 0, SNAPKV_FP32 = 1 } snapkv_dtype;
+
+/*
+ * Problem shape shared by all calls.
+ *   batch        B >= 1 sequences (at most 4096)
+ *   num_q_heads  H_q >= 1
+ *   num_kv_heads H_kv >= 1, H_q % H_kv == 0 (g = H_q / H_kv)
+ *   head_dim     d, one of 64 or 128
+ *   dtype        element type of q_win, k, v, out_k, out_v (snapkv_dtype)
+ */
+typedef struct {
+    int32_t batch;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t dtype;
+} snapkv_shape;
+
+/*
+ * Bytes of device workspace snapkv_compress needs for this problem.
+ * seqlens_host: host array of B prompt lengths.  Returns 0 if the arguments
+ * are invalid (the same checks snapkv_compress makes).
+ */
+size_t snapkv_workspace_size(const snapkv_shape *shape, const int32_t *seqlens_host,
+                             int32_t W, int32_t C);
+
+/*
+ * Compress one layer's prompt KV cache.
+ *
+ * Inputs (device, 16-byte aligned, element type shape->dtype):
+ *   q_win  [B, W, H_q, d]  queries of positions L_b-W .. L_b-1 of each
+ *                          sequence, exactly as the layer's attention uses
+ *                          them (position encoding already applied)
+ *   k, v   [T, H_kv, d]    packed prompt keys / values, T = sum of seqlens;
+ *                          sequence b owns rows off_b .. off_b + L_b - 1 with
+ *                          off_b = L_0 + ... + L_{b-1}
+ * seqlens_host: host array of B lengths, each >= 1.
+ * W >= 1 (window), C >= W (total budget per sequence and KV head),
+ * kernel_size odd and >= 1 (1 = no pooling), pool_type a snapkv_pool.
+ *
+ * Outputs (device, 16-byte aligned):
+ *   out_k, out_v [B, C, H_kv, d]  slot s of (b, h) holds the row of position
+ *                                 out_idx[b, h, s]; slots with index -1 are
+ *                                 zero-filled
+ *   out_idx      [B, H_kv, C]     int32 positions within the sequence: the
+ *                                 C - W kept prefix positions ascending, then
+ *                                 L_b - W .. L_b - 1.  If L_b <= C: 0 .. L_b-1
+ *                                 then -1.
+ * workspace: device, 256-byte aligned, at least snapkv_workspace_size bytes.
+ *
+ * Errors: SNAPKV_ERR_INVALID_ARG for a null pointer, B < 1 or > 4096, any
+ * L_b < 1, H_q % H_kv != 0, W < 1, C < W, an even or non-positive
+ * kernel_size, an unknown pool_type or dtype, or a misaligned buffer;
+ * SNAPKV_ERR_UNSUPPORTED for d not in {64, 128} or W * g > 256;
+ * SNAPKV_ERR_WORKSPACE if workspace_bytes is too small; SNAPKV_ERR_CUDA if a
+ * launch fails.  Nothing is enqueued when an error is returned.
+ */
+int snapkv_compress(const snapkv_shape *shape, const void *q_win, const void *k,
+                    const void *v, const int32_t *seqlens_host, int32_t W,
+                    int32_t kernel_size, int32_t pool_type, int32_t C, void *out_k,
+                    void *out_v, int32_t *out_idx, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/*
+ * Only the scoring step of snapkv_compress (window attention sums with the
+ * GQA mean; no pooling, selection or emission), with the same meaning of
+ * every argument.  The raw scores land in the workspace where
+ * snapkv_score_offsets says; the pooled-score region is not touched.
+ * Useful on its own (score inspection) and to time the score kernel alone.
+ * Errors as for snapkv_compress.
+ */
+int snapkv_score(const snapkv_shape *shape, const void *q_win, const void *k,
+                 const int32_t *seqlens_host, int32_t W, int32_t C, void *workspace,
+                 size_t workspace_bytes, void *stream);
+
+/*
+ * Where the last snapkv_compress on this workspace left its fp32 score
+ * vectors.  For every sequence with L_b > C and every KV head, the P_b =
+ * L_b - W raw scores (window sums, group mean) and pooled scores are packed
+ * in (b, h, j) order; a sequence with L_b <= C has no scores and takes no
+ * room.  *raw_offset / *pooled_offset receive byte offsets into the
+ * workspace; *count receives the number of floats in each vector.
+ */
+int snapkv_score_offsets(const snapkv_shape *shape, const int32_t *seqlens_host, int32_t W,
+                         int32_t C, size_t *raw_offset, size_t *pooled_offset,
+                         size_t *count);
+
+/*
+ * Synchronize `stream`, then read the device status word that the kernels
+ * of the last snapkv_compress on this workspace wrote: SNAPKV_OK, or
+ * SNAPKV_ERR_TIMEOUT if a bounded device-side wait gave up.
+ */
+int snapkv_get_status(const void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Host-buffer variant.  Inputs and outputs are host arrays with the layouts
+ * of snapkv_compress (page-locked memory makes the copies asynchronous and
+ * fast).  The call copies q_win, k and v to `staging` on the device, runs
+ * snapkv_compress there, copies out_k, out_v and out_idx back and waits for
+ * the stream, so the outputs are complete when it returns.  staging: device,
+ * 256-byte aligned, at least snapkv_host_staging_size bytes.
+ */
+size_t snapkv_host_staging_size(const snapkv_shape *shape, const int32_t *seqlens_host,
+                                int32_t W, int32_t C);
+
+int snapkv_compress_host(const snapkv_shape *shape, const void *q_win_host,
+                         const void *k_host, const void *v_host,
+                         const int32_t *seqlens_host, int32_t W, int32_t kernel_size,
+                         int32_t pool_type, int32_t C, void *out_k_host, void *out_v_host,
+                         int32_t *out_idx_host, void *staging, size_t staging_bytes,
+                         void *stream);
+
+/*
+ * Number of CUDA kernels this library has launched in this process so far
+ * (all devices, all streams), for launch accounting.
+ */
+uint64_t snapkv_kernel_launches(void);
+
+/* Static text for a status code. */
+const char *snapkv_status_string(int status);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int snapkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SNAPKV_H */

@@ -1,0 +1,9 @@
+"""SnapKV prefill-time KV-cache compression for GB300 (sm_103a).
+
+The compute lives in libsnapkv.so (hand-written CUDA, C ABI in
+include/snapkv.h); ``snapkv`` is its thin ctypes binding.
+"""
+from . import snapkv  # noqa: F401
+from .snapkv import SnapKVConfig, compress, compress_host, load  # noqa: F401
+
+__version__ = "0.1.0"

@@ -1,0 +1,65 @@
+// Internal launch plan shared by the host side and the kernels of libsnapkv.
+//
+// A call is split into groups of at most kGroupSeqs sequences; each group's
+// per-sequence table travels to the kernels by value as a __grid_constant__
+// parameter, so a launch needs no host-to-device copy and no allocation.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace snapkv {
+
+constexpr int kGroupSeqs = 64;     // sequences per launch group
+constexpr int kMaxRows = 256;      // W * g limit (query rows per KV head)
+constexpr int kMaxBatch = 4096;
+constexpr int kClusterCTAs = 8;    // CTAs per (sequence, KV head) in select/gather
+constexpr int kSelectThreads = 512;
+
+// Status word values written by kernels (0 = fine).
+constexpr int kDevOk = 0;
+constexpr int kDevTimeout = 5;
+
+struct SeqInfo {
+  int b;             // index of the sequence in the caller's batch
+  int L;             // prompt length
+  int P;             // L - W (prefix length; may be <= 0)
+  int scored;        // 1 if L > C: scores, pooling and selection run
+  long long row0;    // first packed row of this sequence in k / v
+  long long score0;  // float offset of (b, h=0) in raw / pooled; (b,h) at score0 + h*P
+  int piece0;        // first score piece of this sequence (group-local)
+  int chunks;        // score pieces per KV head
+};
+
+struct Plan {
+  // problem
+  int nseq;          // sequences in this group
+  int H_q, H_kv, g, d, W, Wp, C, n, kp, pool, dtype;
+  float scale;       // 1 / sqrt(d)
+  float log2e_scale; // log2(e) / sqrt(d)
+  // score pieces (pass 1 and pass 2 share them)
+  int chunk_keys;
+  int total_pieces;
+  // buffers
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out_k;
+  void* out_v;
+  int32_t* out_idx;
+  float* raw;        // [sum P] packed (b, h, j)
+  float* pooled;     // same packing
+  float2* stats;     // [total_pieces * Wp] (running max, sum of exp) per piece and row
+  float* lse;        // [nseq * H_kv * Wp] natural-log LSE per (sequence, head, row)
+  int* status;       // device status word
+  SeqInfo seq[kGroupSeqs];
+};
+
+// Adds n to the library's process-wide kernel-launch counter.
+void count_launches(int n);
+
+// Launchers (each returns a cudaError_t as int).
+int launch_score_simt(const Plan& p, void* stream);
+int launch_select_gather(const Plan& p, void* stream);
+
+}  // namespace snapkv

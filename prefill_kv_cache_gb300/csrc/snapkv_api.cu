@@ -1,0 +1,311 @@
+// C ABI of libsnapkv: argument checks, workspace layout, launch planning.
+//
+// Every entry point is declared, with its contract, in include/snapkv.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "plan.h"
+#include "snapkv.h"
+
+namespace snapkv {
+
+int launch_score_tc(const Plan& p, void* stream, bool* taken);
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr int kChunkKeys = 1024;  // keys per score piece
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t status = 0;  // int status word
+  size_t raw = 0, pooled = 0, stats = 0, lse = 0;
+  size_t score_count = 0;  // floats in raw (and in pooled)
+  size_t total = 0;
+};
+
+// Checks shared by every entry point; SNAPKV_OK when the problem is valid
+// and supported.
+int check_problem(const snapkv_shape* sh, const int32_t* seqlens, int W, int C) {
+  if (!sh || !seqlens) return SNAPKV_ERR_INVALID_ARG;
+  if (sh->batch < 1 || sh->batch > kMaxBatch) return SNAPKV_ERR_INVALID_ARG;
+  if (sh->num_q_heads < 1 || sh->num_kv_heads < 1) return SNAPKV_ERR_INVALID_ARG;
+  if (sh->num_q_heads % sh->num_kv_heads) return SNAPKV_ERR_INVALID_ARG;
+  if (sh->dtype != SNAPKV_BF16 && sh->dtype != SNAPKV_FP32) return SNAPKV_ERR_INVALID_ARG;
+  if (W < 1 || C < W) return SNAPKV_ERR_INVALID_ARG;
+  for (int b = 0; b < sh->batch; ++b)
+    if (seqlens[b] < 1) return SNAPKV_ERR_INVALID_ARG;
+  if (sh->head_dim != 64 && sh->head_dim != 128) return SNAPKV_ERR_UNSUPPORTED;
+  const long long Wp = (long long)W * (sh->num_q_heads / sh->num_kv_heads);
+  if (Wp > kMaxRows) return SNAPKV_ERR_UNSUPPORTED;
+  return SNAPKV_OK;
+}
+
+int chunks_for(int L) { return (L + kChunkKeys - 1) / kChunkKeys; }
+
+Layout layout_for(const snapkv_shape* sh, const int32_t* seqlens, int W, int C) {
+  Layout lay;
+  const int H = sh->num_kv_heads;
+  const int Wp = W * (sh->num_q_heads / H);
+  size_t scores = 0, max_pieces = 0, max_units = 0;
+  for (int g0 = 0; g0 < sh->batch; g0 += kGroupSeqs) {
+    const int g1 = std::min(sh->batch, g0 + kGroupSeqs);
+    size_t pieces = 0;
+    for (int b = g0; b < g1; ++b) {
+      if (seqlens[b] > C) {
+        scores += (size_t)H * (seqlens[b] - W);
+        pieces += (size_t)H * chunks_for(seqlens[b]);
+      }
+    }
+    max_pieces = std::max(max_pieces, pieces);
+    max_units = std::max(max_units, (size_t)(g1 - g0) * H);
+  }
+  size_t off = 0;
+  lay.status = off;
+  off += kAlign;
+  lay.raw = off;
+  off = align_up(off + scores * sizeof(float));
+  lay.pooled = off;
+  off = align_up(off + scores * sizeof(float));
+  lay.stats = off;
+  off = align_up(off + max_pieces * Wp * sizeof(float2));
+  lay.lse = off;
+  off = align_up(off + max_units * Wp * sizeof(float));
+  lay.score_count = scores;
+  lay.total = off;
+  return lay;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace snapkv
+
+using namespace snapkv;
+
+extern "C" {
+
+const char* snapkv_status_string(int status) {
+  switch (status) {
+    case SNAPKV_OK: return "ok";
+    case SNAPKV_ERR_INVALID_ARG: return "invalid argument";
+    case SNAPKV_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case SNAPKV_ERR_WORKSPACE: return "workspace too small";
+    case SNAPKV_ERR_CUDA: return "CUDA error";
+    case SNAPKV_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int snapkv_version(void) { return 0x000100; }
+
+size_t snapkv_workspace_size(const snapkv_shape* shape, const int32_t* seqlens_host, int32_t W,
+                             int32_t C) {
+  if (check_problem(shape, seqlens_host, W, C) != SNAPKV_OK) return 0;
+  return layout_for(shape, seqlens_host, W, C).total;
+}
+
+int snapkv_score_offsets(const snapkv_shape* shape, const int32_t* seqlens_host, int32_t W,
+                         int32_t C, size_t* raw_offset, size_t* pooled_offset, size_t* count) {
+  const int rc = check_problem(shape, seqlens_host, W, C);
+  if (rc != SNAPKV_OK) return rc;
+  if (!raw_offset || !pooled_offset || !count) return SNAPKV_ERR_INVALID_ARG;
+  const Layout lay = layout_for(shape, seqlens_host, W, C);
+  *raw_offset = lay.raw;
+  *pooled_offset = lay.pooled;
+  *count = lay.score_count;
+  return SNAPKV_OK;
+}
+
+namespace {
+
+// Shared by snapkv_compress (score_only = false) and snapkv_score.
+int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const void* v,
+            const int32_t* seqlens_host, int32_t W, int32_t kernel_size, int32_t pool_type,
+            int32_t C, void* out_k, void* out_v, int32_t* out_idx, void* workspace,
+            size_t workspace_bytes, void* stream, bool score_only) {
+  int rc = check_problem(shape, seqlens_host, W, C);
+  if (rc == SNAPKV_ERR_INVALID_ARG) return rc;
+  if (!q_win || !k || !workspace) return SNAPKV_ERR_INVALID_ARG;
+  if (!aligned(q_win, 16) || !aligned(k, 16) || !aligned(workspace, kAlign))
+    return SNAPKV_ERR_INVALID_ARG;
+  if (!score_only) {
+    if (!v || !out_k || !out_v || !out_idx) return SNAPKV_ERR_INVALID_ARG;
+    if (kernel_size < 1 || kernel_size % 2 == 0) return SNAPKV_ERR_INVALID_ARG;
+    if (pool_type != SNAPKV_POOL_AVG && pool_type != SNAPKV_POOL_MAX)
+      return SNAPKV_ERR_INVALID_ARG;
+    if (!aligned(v, 16) || !aligned(out_k, 16) || !aligned(out_v, 16) || !aligned(out_idx, 16))
+      return SNAPKV_ERR_INVALID_ARG;
+  }
+  if (rc != SNAPKV_OK) return rc;
+  const Layout lay = layout_for(shape, seqlens_host, W, C);
+  if (workspace_bytes < lay.total) return SNAPKV_ERR_WORKSPACE;
+
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws + lay.status, 0, sizeof(int), st) != cudaSuccess) return SNAPKV_ERR_CUDA;
+
+  const int H = shape->num_kv_heads;
+  Plan p;
+  std::memset(&p, 0, sizeof p);
+  p.H_q = shape->num_q_heads;
+  p.H_kv = H;
+  p.g = p.H_q / H;
+  p.d = shape->head_dim;
+  p.W = W;
+  p.Wp = W * p.g;
+  p.C = C;
+  p.n = C - W;
+  p.kp = kernel_size;
+  p.pool = pool_type;
+  p.dtype = shape->dtype;
+  p.scale = (float)(1.0 / std::sqrt((double)p.d));
+  p.log2e_scale = (float)(1.4426950408889634 / std::sqrt((double)p.d));
+  p.chunk_keys = kChunkKeys;
+  p.q = q_win;
+  p.k = k;
+  p.v = v;
+  p.out_k = out_k;
+  p.out_v = out_v;
+  p.out_idx = out_idx;
+  p.raw = reinterpret_cast<float*>(ws + lay.raw);
+  p.pooled = reinterpret_cast<float*>(ws + lay.pooled);
+  p.stats = reinterpret_cast<float2*>(ws + lay.stats);
+  p.lse = reinterpret_cast<float*>(ws + lay.lse);
+  p.status = reinterpret_cast<int*>(ws + lay.status);
+
+  long long row0 = 0, score0 = 0;
+  for (int g0 = 0; g0 < shape->batch; g0 += kGroupSeqs) {
+    const int g1 = std::min(shape->batch, g0 + kGroupSeqs);
+    p.nseq = g1 - g0;
+    int piece = 0;
+    for (int b = g0; b < g1; ++b) {
+      SeqInfo& S = p.seq[b - g0];
+      S.b = b;
+      S.L = seqlens_host[b];
+      S.P = S.L - W;
+      S.scored = S.L > C;
+      S.row0 = row0;
+      S.score0 = score0;
+      S.piece0 = piece;
+      S.chunks = S.scored ? chunks_for(S.L) : 0;
+      piece += S.chunks * H;
+      if (S.scored) score0 += (long long)H * S.P;
+      row0 += S.L;
+    }
+    p.total_pieces = piece;
+    if (piece > 0) {
+      bool taken = false;
+      if (launch_score_tc(p, stream, &taken) != cudaSuccess) return SNAPKV_ERR_CUDA;
+      if (!taken && launch_score_simt(p, stream) != cudaSuccess) return SNAPKV_ERR_CUDA;
+    }
+    if (!score_only && launch_select_gather(p, stream) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  }
+  return SNAPKV_OK;
+}
+
+}  // namespace
+
+int snapkv_compress(const snapkv_shape* shape, const void* q_win, const void* k, const void* v,
+                    const int32_t* seqlens_host, int32_t W, int32_t kernel_size,
+                    int32_t pool_type, int32_t C, void* out_k, void* out_v, int32_t* out_idx,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  return enqueue(shape, q_win, k, v, seqlens_host, W, kernel_size, pool_type, C, out_k, out_v,
+                 out_idx, workspace, workspace_bytes, stream, false);
+}
+
+int snapkv_score(const snapkv_shape* shape, const void* q_win, const void* k,
+                 const int32_t* seqlens_host, int32_t W, int32_t C, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  return enqueue(shape, q_win, k, nullptr, seqlens_host, W, 1, SNAPKV_POOL_AVG, C, nullptr,
+                 nullptr, nullptr, workspace, workspace_bytes, stream, true);
+}
+
+uint64_t snapkv_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int snapkv_get_status(const void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < sizeof(int)) return SNAPKV_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SNAPKV_ERR_CUDA;
+  return word == kDevOk ? SNAPKV_OK : SNAPKV_ERR_TIMEOUT;
+}
+
+// Host-buffer variant: staging holds q, k, v, out_k, out_v, out_idx, workspace.
+namespace {
+struct HostLayout {
+  size_t q, k, v, ok, ov, oi, ws, ws_bytes, total;
+  size_t q_bytes, kv_bytes, out_bytes, idx_bytes;
+};
+
+HostLayout host_layout(const snapkv_shape* sh, const int32_t* seqlens, int W, int C) {
+  HostLayout h{};
+  const size_t esz = sh->dtype == SNAPKV_BF16 ? 2 : 4;
+  long long T = 0;
+  for (int b = 0; b < sh->batch; ++b) T += seqlens[b];
+  h.q_bytes = (size_t)sh->batch * W * sh->num_q_heads * sh->head_dim * esz;
+  h.kv_bytes = (size_t)T * sh->num_kv_heads * sh->head_dim * esz;
+  h.out_bytes = (size_t)sh->batch * C * sh->num_kv_heads * sh->head_dim * esz;
+  h.idx_bytes = (size_t)sh->batch * sh->num_kv_heads * C * sizeof(int32_t);
+  size_t off = 0;
+  h.q = off; off = align_up(off + h.q_bytes);
+  h.k = off; off = align_up(off + h.kv_bytes);
+  h.v = off; off = align_up(off + h.kv_bytes);
+  h.ok = off; off = align_up(off + h.out_bytes);
+  h.ov = off; off = align_up(off + h.out_bytes);
+  h.oi = off; off = align_up(off + h.idx_bytes);
+  h.ws = off;
+  h.ws_bytes = layout_for(sh, seqlens, W, C).total;
+  h.total = off + h.ws_bytes;
+  return h;
+}
+}  // namespace
+
+size_t snapkv_host_staging_size(const snapkv_shape* shape, const int32_t* seqlens_host,
+                                int32_t W, int32_t C) {
+  if (check_problem(shape, seqlens_host, W, C) != SNAPKV_OK) return 0;
+  return host_layout(shape, seqlens_host, W, C).total;
+}
+
+int snapkv_compress_host(const snapkv_shape* shape, const void* q_win_host, const void* k_host,
+                         const void* v_host, const int32_t* seqlens_host, int32_t W,
+                         int32_t kernel_size, int32_t pool_type, int32_t C, void* out_k_host,
+                         void* out_v_host, int32_t* out_idx_host, void* staging,
+                         size_t staging_bytes, void* stream) {
+  int rc = check_problem(shape, seqlens_host, W, C);
+  if (rc != SNAPKV_OK) return rc;
+  if (!q_win_host || !k_host || !v_host || !out_k_host || !out_v_host || !out_idx_host ||
+      !staging || !aligned(staging, kAlign))
+    return SNAPKV_ERR_INVALID_ARG;
+  const HostLayout h = host_layout(shape, seqlens_host, W, C);
+  if (staging_bytes < h.total) return SNAPKV_ERR_WORKSPACE;
+  char* base = static_cast<char*>(staging);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(base + h.q, q_win_host, h.q_bytes, cudaMemcpyHostToDevice, st) ||
+      cudaMemcpyAsync(base + h.k, k_host, h.kv_bytes, cudaMemcpyHostToDevice, st) ||
+      cudaMemcpyAsync(base + h.v, v_host, h.kv_bytes, cudaMemcpyHostToDevice, st))
+    return SNAPKV_ERR_CUDA;
+  rc = snapkv_compress(shape, base + h.q, base + h.k, base + h.v, seqlens_host, W, kernel_size,
+                       pool_type, C, base + h.ok, base + h.ov,
+                       reinterpret_cast<int32_t*>(base + h.oi), base + h.ws, h.ws_bytes, stream);
+  if (rc != SNAPKV_OK) return rc;
+  if (cudaMemcpyAsync(out_k_host, base + h.ok, h.out_bytes, cudaMemcpyDeviceToHost, st) ||
+      cudaMemcpyAsync(out_v_host, base + h.ov, h.out_bytes, cudaMemcpyDeviceToHost, st) ||
+      cudaMemcpyAsync(out_idx_host, base + h.oi, h.idx_bytes, cudaMemcpyDeviceToHost, st))
+    return SNAPKV_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  return SNAPKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,255 @@
+"""Python binding of libsnapkv (ctypes; argument marshalling only).
+
+Every step of the compression runs in the library's CUDA kernels; this module
+only turns torch tensors into pointers, sizes and a stream handle.  If the
+shared library is missing it raises: there is no Python or CPU fallback.
+
+Keyword names follow the SnapKV usage example on the jisaku.com glossary page
+"SnapKV" (section "実装と統合"): window_size, max_capacity_prompt, kernel_size,
+pooling ("avgpool" / "maxpool").
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libsnapkv.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(6)
+POOL_AVG, POOL_MAX = 0, 1
+BF16, FP32 = 0, 1
+
+EXPORTED = (
+    "snapkv_workspace_size",
+    "snapkv_compress",
+    "snapkv_score",
+    "snapkv_score_offsets",
+    "snapkv_get_status",
+    "snapkv_host_staging_size",
+    "snapkv_compress_host",
+    "snapkv_kernel_launches",
+    "snapkv_status_string",
+    "snapkv_version",
+)
+
+
+class SnapKVError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} ({code})" if what else status_string(code))
+
+
+class snapkv_shape(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load libsnapkv.so (built by __graft_entry__.build()); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libsnapkv.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+    shp = ctypes.POINTER(snapkv_shape)
+    lib.snapkv_workspace_size.argtypes = [shp, vp, i32, i32]
+    lib.snapkv_workspace_size.restype = sz
+    lib.snapkv_compress.argtypes = [shp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]
+    lib.snapkv_compress.restype = ctypes.c_int
+    lib.snapkv_score.argtypes = [shp, vp, vp, vp, i32, i32, vp, sz, vp]
+    lib.snapkv_score.restype = ctypes.c_int
+    lib.snapkv_kernel_launches.argtypes = []
+    lib.snapkv_kernel_launches.restype = ctypes.c_uint64
+    lib.snapkv_score_offsets.argtypes = [shp, vp, i32, i32, ctypes.POINTER(sz),
+                                         ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    lib.snapkv_score_offsets.restype = ctypes.c_int
+    lib.snapkv_get_status.argtypes = [vp, sz, vp]
+    lib.snapkv_get_status.restype = ctypes.c_int
+    lib.snapkv_host_staging_size.argtypes = [shp, vp, i32, i32]
+    lib.snapkv_host_staging_size.restype = sz
+    lib.snapkv_compress_host.argtypes = [shp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
+                                         vp, sz, vp]
+    lib.snapkv_compress_host.restype = ctypes.c_int
+    lib.snapkv_status_string.argtypes = [ctypes.c_int]
+    lib.snapkv_status_string.restype = ctypes.c_char_p
+    lib.snapkv_version.argtypes = []
+    lib.snapkv_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load().snapkv_status_string(int(code)).decode()
+
+
+def pool_code(pooling) -> int:
+    if pooling in ("avgpool", "avg", POOL_AVG):
+        return POOL_AVG
+    if pooling in ("maxpool", "max", POOL_MAX):
+        return POOL_MAX
+    raise ValueError(f"unknown pooling {pooling!r}")
+
+
+def dtype_code(dtype) -> int:
+    if dtype == torch.bfloat16:
+        return BF16
+    if dtype == torch.float32:
+        return FP32
+    raise TypeError(f"unsupported dtype {dtype}")
+
+
+@dataclasses.dataclass
+class SnapKVConfig:
+    """The four knobs of the pages' usage example, with its default values."""
+    window_size: int = 32
+    max_capacity_prompt: int = 4096
+    kernel_size: int = 5
+    pooling: str = "avgpool"
+
+
+def _seqlens_array(seqlens):
+    vals = [int(x) for x in seqlens]
+    arr = (ctypes.c_int32 * len(vals))(*vals)
+    return arr, len(vals)
+
+
+def make_shape(batch, num_q_heads, num_kv_heads, head_dim, dtype) -> snapkv_shape:
+    return snapkv_shape(int(batch), int(num_q_heads), int(num_kv_heads), int(head_dim),
+                        dtype if isinstance(dtype, int) else dtype_code(dtype))
+
+
+def workspace_size(shape: snapkv_shape, seqlens, window_size: int, max_capacity_prompt: int) -> int:
+    arr, _ = _seqlens_array(seqlens)
+    return int(load().snapkv_workspace_size(ctypes.byref(shape), arr, int(window_size),
+                                            int(max_capacity_prompt)))
+
+
+def score_offsets(shape: snapkv_shape, seqlens, window_size: int, max_capacity_prompt: int):
+    arr, _ = _seqlens_array(seqlens)
+    r, p, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    rc = load().snapkv_score_offsets(ctypes.byref(shape), arr, int(window_size),
+                                     int(max_capacity_prompt), ctypes.byref(r), ctypes.byref(p),
+                                     ctypes.byref(c))
+    if rc:
+        raise SnapKVError(rc, "snapkv_score_offsets")
+    return r.value, p.value, c.value
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def compress(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seqlens,
+             window_size: int, kernel_size: int, pooling, max_capacity_prompt: int,
+             out_k: torch.Tensor | None = None, out_v: torch.Tensor | None = None,
+             out_idx: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+             stream=None):
+    """Compress one layer (see include/snapkv.h, snapkv_compress).
+
+    q_win [B, W, H_q, d], k / v [T, H_kv, d] (packed, bf16 or fp32, CUDA);
+    seqlens: B host integers.  Returns (out_k, out_v, out_idx, workspace);
+    outputs that are not given are allocated here with torch.
+    """
+    B, W, H_q, d = q_win.shape
+    H_kv = k.shape[1]
+    C = int(max_capacity_prompt)
+    if W != int(window_size):
+        raise ValueError("q_win's second dimension must equal window_size")
+    shape = make_shape(B, H_q, H_kv, d, q_win.dtype)
+    if out_k is None:
+        out_k = torch.empty((B, C, H_kv, d), dtype=k.dtype, device=k.device)
+    if out_v is None:
+        out_v = torch.empty((B, C, H_kv, d), dtype=k.dtype, device=k.device)
+    if out_idx is None:
+        out_idx = torch.empty((B, H_kv, C), dtype=torch.int32, device=k.device)
+    ws_bytes = workspace_size(shape, seqlens, W, C)
+    if ws_bytes == 0:
+        raise SnapKVError(ERR_INVALID_ARG, "snapkv_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=k.device)
+    for name, t in (("q_win", q_win), ("k", k), ("v", v), ("out_k", out_k), ("out_v", out_v),
+                    ("out_idx", out_idx), ("workspace", workspace)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    arr, _ = _seqlens_array(seqlens)
+    rc = load().snapkv_compress(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                arr, W, int(kernel_size), pool_code(pooling), C,
+                                out_k.data_ptr(), out_v.data_ptr(), out_idx.data_ptr(),
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _stream_handle(stream))
+    if rc:
+        raise SnapKVError(rc, "snapkv_compress")
+    return out_k, out_v, out_idx, workspace
+
+
+def score(q_win: torch.Tensor, k: torch.Tensor, seqlens, window_size: int,
+          max_capacity_prompt: int, workspace: torch.Tensor, stream=None) -> None:
+    """Scoring step only (include/snapkv.h, snapkv_score); raw scores stay in workspace."""
+    B, W, H_q, d = q_win.shape
+    shape = make_shape(B, H_q, k.shape[1], d, q_win.dtype)
+    arr, _ = _seqlens_array(seqlens)
+    rc = load().snapkv_score(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(), arr, W,
+                             int(max_capacity_prompt), workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc:
+        raise SnapKVError(rc, "snapkv_score")
+
+
+def kernel_launches() -> int:
+    return int(load().snapkv_kernel_launches())
+
+
+def get_status(workspace: torch.Tensor, stream=None) -> int:
+    return int(load().snapkv_get_status(workspace.data_ptr(),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream_handle(stream)))
+
+
+def scores_from_workspace(workspace: torch.Tensor, shape: snapkv_shape, seqlens,
+                          window_size: int, max_capacity_prompt: int):
+    """(raw, pooled) fp32 views into the workspace after a compress call."""
+    r, p, c = score_offsets(shape, seqlens, window_size, max_capacity_prompt)
+    raw = workspace[r:r + 4 * c].view(torch.float32)
+    pooled = workspace[p:p + 4 * c].view(torch.float32)
+    return raw, pooled
+
+
+def host_staging_size(shape: snapkv_shape, seqlens, window_size: int,
+                      max_capacity_prompt: int) -> int:
+    arr, _ = _seqlens_array(seqlens)
+    return int(load().snapkv_host_staging_size(ctypes.byref(shape), arr, int(window_size),
+                                               int(max_capacity_prompt)))
+
+
+def compress_host(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seqlens,
+                  window_size: int, kernel_size: int, pooling, max_capacity_prompt: int,
+                  out_k: torch.Tensor, out_v: torch.Tensor, out_idx: torch.Tensor,
+                  staging: torch.Tensor, stream=None) -> None:
+    """Host-buffer variant (include/snapkv.h, snapkv_compress_host).
+
+    All tensors but `staging` are CPU tensors (pinned for speed); `staging`
+    is a CUDA uint8 tensor of at least host_staging_size bytes.  Returns when
+    the outputs are complete.
+    """
+    B, W, H_q, d = q_win.shape
+    shape = make_shape(B, H_q, k.shape[1], d, q_win.dtype)
+    arr, _ = _seqlens_array(seqlens)
+    rc = load().snapkv_compress_host(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(),
+                                     v.data_ptr(), arr, W, int(kernel_size), pool_code(pooling),
+                                     int(max_capacity_prompt), out_k.data_ptr(), out_v.data_ptr(),
+                                     out_idx.data_ptr(), staging.data_ptr(), staging.numel(),
+                                     _stream_handle(stream))
+    if rc:
+        raise SnapKVError(rc, "snapkv_compress_host")

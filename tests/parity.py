@@ -1,0 +1,127 @@
+"""GPU-vs-oracle agreement rule, shared by the GPU parity tests.
+
+Rule (scores fp32 on the GPU, fp64 in the oracle):
+  * pooled (and raw) scores: |gpu - oracle| <= 1e-7 + 1e-5 * |oracle|;
+  * with tau the oracle's (C-W)-th best pooled score, the exemption set is
+    E = {j : |pooled_oracle[j] - tau| <= 1e-5 * tau}; the kept prefix sets of
+    GPU and oracle may differ only inside E (the count is reported);
+  * every GPU output slot holds the exact bytes of the K and V rows of its
+    own index (compared by index, since an exempt swap shifts later slots);
+    unused slots (index -1) are zero; the kept prefix indices ascend; the
+    window block is identical to the oracle's.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from prefill_kv_cache_gb300 import snapkv as S
+
+RTOL = 1e-5
+ATOL = 1e-7
+
+
+def to_device(a: np.ndarray, dev="cuda") -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if a.dtype == np.uint16:
+        t = t.view(torch.bfloat16)
+    return t.to(dev)
+
+
+def run_gpu(lay, k_pool, pool, C, dev="cuda"):
+    """One snapkv_compress on the layer; returns numpy outputs and scores."""
+    q = to_device(lay.q_win, dev)
+    k = to_device(lay.k, dev)
+    v = to_device(lay.v, dev)
+    ok, ov, oi, ws = S.compress(q, k, v, lay.seqlens, lay.W, k_pool, pool, C)
+    st = S.get_status(ws)
+    assert st == S.OK, S.status_string(st)
+    shape = S.make_shape(lay.B, lay.H_q, lay.H_kv, lay.d, q.dtype)
+    raw, pooled = S.scores_from_workspace(ws, shape, lay.seqlens, lay.W, C)
+    torch.cuda.synchronize()
+
+    def host(t):
+        t = t.cpu()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+    return dict(out_k=host(ok), out_v=host(ov), idx=oi.cpu().numpy(), raw=raw.cpu().numpy(),
+                pooled=pooled.cpu().numpy())
+
+
+def unpack_scores(vec, seqlens, H_kv, W, C):
+    """Split a packed (b, h, j) score vector into per-sequence [H_kv, P] arrays."""
+    out, off = [], 0
+    for L in seqlens:
+        L = int(L)
+        if L > C:
+            P = L - W
+            out.append(vec[off:off + H_kv * P].reshape(H_kv, P))
+            off += H_kv * P
+        else:
+            out.append(None)
+    return out
+
+
+def check(lay, gpu, ora, C, seqs=None, heads=None, report=None):
+    """Assert the agreement rule on sequences `seqs` (default all) of `lay`.
+
+    `ora` holds the oracle's outputs for exactly those sequences, in order.
+    Returns the number of exempt swaps seen.
+    """
+    W, H_kv = lay.W, lay.H_kv
+    n = C - W
+    seqs = list(range(lay.B)) if seqs is None else list(seqs)
+    heads = list(range(H_kv)) if heads is None else list(heads)
+    g_raw = unpack_scores(gpu["raw"], lay.seqlens, H_kv, W, C)
+    g_pool = unpack_scores(gpu["pooled"], lay.seqlens, H_kv, W, C)
+    offs = lay.offsets
+    swaps = 0
+    for oi_, b in enumerate(seqs):
+        L = int(lay.seqlens[b])
+        P = L - W
+        for h in heads:
+            gi = gpu["idx"][b, h]
+            oi = ora["idx"][oi_, h]
+            tag = f"seq {b} head {h}"
+            if L > C:
+                np.testing.assert_allclose(g_raw[b][h], ora["raw"][oi_][h], rtol=RTOL, atol=ATOL,
+                                           err_msg=f"raw scores, {tag}")
+                np.testing.assert_allclose(g_pool[b][h], ora["pooled"][oi_][h], rtol=RTOL,
+                                           atol=ATOL, err_msg=f"pooled scores, {tag}")
+                assert gi[n:].tolist() == list(range(P, L)), f"window block, {tag}"
+                sel_g = gi[:n]
+                assert (np.diff(sel_g) > 0).all() and sel_g.min(initial=0) >= 0 and \
+                    sel_g.max(initial=0) < P, f"kept indices not ascending in [0,P), {tag}"
+                tau = ora["tau"][oi_, h]
+                po = ora["pooled"][oi_][h]
+                diff = set(sel_g.tolist()) ^ set(oi[:n].tolist())
+                if diff:
+                    bad = [j for j in diff if abs(po[j] - tau) > RTOL * tau]
+                    assert not bad, f"kept sets differ outside the exemption band, {tag}: {bad[:8]}"
+                    swaps += len(diff) // 2
+            else:
+                assert gi.tolist() == oi.tolist(), f"keep-all indices, {tag}"
+            # bytes by index
+            rows = gi >= 0
+            src = offs[b] + gi[rows]
+            np.testing.assert_array_equal(gpu["out_k"][b, rows, h], lay.k[src, h], err_msg=tag)
+            np.testing.assert_array_equal(gpu["out_v"][b, rows, h], lay.v[src, h], err_msg=tag)
+            assert (gpu["out_k"][b, ~rows, h] == 0).all() and (gpu["out_v"][b, ~rows, h] == 0).all()
+    if report is not None:
+        report.append(swaps)
+    return swaps
+
+
+def oracle_for(lay, k_pool, pool, C, seqs=None, nthreads=None):
+    """Oracle outputs on a subset of sequences (default all)."""
+    if seqs is None:
+        return oracle.compress(lay.q_win, lay.k, lay.v, lay.seqlens, lay.W, k_pool, pool, C,
+                               nthreads=nthreads)
+    seqs = list(seqs)
+    offs = lay.offsets
+    q = np.ascontiguousarray(lay.q_win[seqs])
+    ks = np.concatenate([lay.k[offs[b]:offs[b] + lay.seqlens[b]] for b in seqs])
+    vs = np.concatenate([lay.v[offs[b]:offs[b] + lay.seqlens[b]] for b in seqs])
+    sl = [int(lay.seqlens[b]) for b in seqs]
+    return oracle.compress(q, ks, vs, sl, lay.W, k_pool, pool, C, nthreads=nthreads)

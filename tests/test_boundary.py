@@ -1,0 +1,115 @@
+"""The C ABI without a GPU: exports, argument checks, workspace sizing.
+
+No call here reaches the CUDA runtime's compute paths: every invalid case is
+rejected by the library before anything is enqueued, and valid-looking cases
+use fake (never dereferenced) pointers only where the library must reject
+them first.
+"""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+
+from prefill_kv_cache_gb300 import snapkv as S
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x10000  # aligned, never dereferenced
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "snapkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(snapkv_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    lib = S.load()
+    names = header_functions()
+    assert set(names) == set(S.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert S.load().snapkv_version() >= 0x000100
+
+
+def shape(B=1, Hq=32, Hkv=8, d=128, dtype=S.BF16):
+    return S.make_shape(B, Hq, Hkv, d, dtype)
+
+
+def compress_rc(sh, seqlens, W=32, k=5, pool=0, C=1024, ptrs=None, ws_bytes=1 << 30,
+                q=FAKE, kk=FAKE, v=FAKE, ok=FAKE, ov=FAKE, oi=FAKE, ws=FAKE):
+    arr = (ctypes.c_int32 * len(seqlens))(*seqlens) if seqlens is not None else None
+    return S.load().snapkv_compress(ctypes.byref(sh) if sh is not None else None, q, kk, v, arr,
+                                    W, k, pool, C, ok, ov, oi, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=None), dict(kk=None), dict(v=None), dict(ok=None), dict(ov=None), dict(oi=None),
+    dict(ws=None), dict(W=0), dict(C=31), dict(k=0), dict(k=4), dict(k=-3), dict(pool=2),
+    dict(q=FAKE + 8), dict(kk=FAKE + 4), dict(ok=FAKE + 2), dict(ws=FAKE + 16),
+])
+def test_invalid_arguments(kw):
+    assert compress_rc(shape(), [4096], **kw) == S.ERR_INVALID_ARG
+
+
+def test_invalid_shapes():
+    assert compress_rc(None, [4096]) == S.ERR_INVALID_ARG
+    assert compress_rc(shape(), None) == S.ERR_INVALID_ARG
+    assert compress_rc(shape(B=0), [4096]) == S.ERR_INVALID_ARG
+    assert compress_rc(shape(B=5000), [4096] * 5000) == S.ERR_INVALID_ARG
+    assert compress_rc(shape(Hq=30), [4096]) == S.ERR_INVALID_ARG
+    assert compress_rc(shape(dtype=7), [4096]) == S.ERR_INVALID_ARG
+    assert compress_rc(shape(B=2), [4096, 0]) == S.ERR_INVALID_ARG
+
+
+def test_unsupported_shapes():
+    assert compress_rc(shape(d=96), [4096]) == S.ERR_UNSUPPORTED
+    assert compress_rc(shape(Hq=64, Hkv=4), [4096], W=32) == S.ERR_UNSUPPORTED  # W*g = 512
+
+
+def test_workspace_too_small():
+    sh = shape()
+    need = S.workspace_size(sh, [20000], 32, 1024)
+    assert need > 0
+    assert compress_rc(sh, [20000], ws_bytes=need - 1) == S.ERR_WORKSPACE
+
+
+def test_workspace_size_invalid_is_zero_and_monotone():
+    sh = shape()
+    assert S.workspace_size(sh, [4096], 0, 1024) == 0
+    assert S.workspace_size(shape(d=96), [4096], 32, 1024) == 0
+    sizes = [S.workspace_size(sh, [L], 32, 1024) for L in (100, 1024, 1025, 5000, 131072)]
+    assert sizes == sorted(sizes)
+    # sequences that fit the budget need no score space
+    assert S.workspace_size(sh, [1024], 32, 1024) == S.workspace_size(sh, [10], 32, 1024)
+
+
+def test_score_offsets_count():
+    sh = shape(B=3)
+    seqlens = [5000, 800, 3000]
+    r, p, c = S.score_offsets(sh, seqlens, 32, 1024)
+    assert c == 8 * (5000 - 32) + 8 * (3000 - 32)
+    assert r % 256 == 0 and p % 256 == 0 and p >= r + 4 * c
+
+
+def test_host_staging_size_covers_buffers():
+    sh = shape()
+    st = S.host_staging_size(sh, [16384], 32, 1024)
+    kv = 16384 * 8 * 128 * 2
+    assert st >= 2 * kv + S.workspace_size(sh, [16384], 32, 1024)
+
+
+def test_status_strings():
+    for code in range(6):
+        assert S.status_string(code)
+    assert S.status_string(99) == "unknown status"
+
+
+def test_binding_defaults_follow_page_example():
+    gold = json.load(open(os.path.join(ROOT, "tests", "golden", "page_parameters.json")))
+    d = gold["api_defaults"]
+    cfg = S.SnapKVConfig()
+    assert (cfg.window_size, cfg.max_capacity_prompt, cfg.kernel_size, cfg.pooling) == (
+        d["window_size"], d["max_capacity_prompt"], d["kernel_size"], d["pooling"])
+    assert S.pool_code("avgpool") == S.POOL_AVG and S.pool_code("maxpool") == S.POOL_MAX

@@ -1,0 +1,131 @@
+"""GPU parity: libsnapkv through its C ABI against the CPU oracle.
+
+Small shapes are compared in full (several tiles, ragged tails, keep-all
+sequences mixed in, every pooling kind and size); the named workloads run at
+full size in the same launch configuration the benchmark times, and the oracle
+checks a sample of their sequences one by one.  The agreement rule is in
+tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from prefill_kv_cache_gb300 import snapkv as S
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_and_check(lay, k_pool, pool, C, seqs=None):
+    gpu = parity.run_gpu(lay, k_pool, pool, C)
+    ora = parity.oracle_for(lay, k_pool, pool, C, seqs=seqs)
+    return parity.check(lay, gpu, ora, C, seqs=seqs), gpu
+
+
+SMALL = [
+    # seqlens,              H_q, H_kv, d,  W,  C,   k, pool,  dtype
+    ([1024],                  4,   4, 64, 16, 256,  5, "avg", "fp32"),
+    ([1025, 300, 2000],       8,   2, 128, 16, 256, 7, "max", "bf16"),
+    ([257, 256, 255, 4000],   4,   1, 64,  8, 256,  1, "avg", "bf16"),
+    ([3000],                 32,   8, 128, 32, 1024, 13, "avg", "bf16"),
+    ([5000, 1100],           32,   8, 128, 32, 1024, 7, "max", "bf16"),
+    ([4097],                 16,   2, 128, 16, 512,  3, "max", "fp32"),
+    ([2049, 33],              8,   8, 64, 32, 32,   5, "avg", "bf16"),   # C == W: no prefix kept
+    ([6000],                 32,   4, 128, 32, 2048, 9, "avg", "bf16"),  # W*g = 256
+    ([1500],                  2,   1, 128, 64, 600, 11, "max", "fp32"),
+    ([33, 17, 1],             4,   2, 64, 16, 40,   5, "avg", "bf16"),   # all keep-all
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"L{c[0]}-g{c[1]//c[2]}-d{c[3]}-W{c[4]}-C{c[5]}-{c[7]}{c[6]}-{c[8]}")
+def test_small_shapes(case):
+    seqlens, H_q, H_kv, d, W, C, kp, pool, dtype = case
+    lay = synth.make_inputs(77 + sum(seqlens), seqlens, H_q, H_kv, d, W, dtype, nspans=3)
+    _run_and_check(lay, kp, pool, C)
+
+
+@pytest.mark.parametrize("pool", ["avg", "max"])
+def test_exact_ties_zero_queries(pool):
+    """q = 0 makes every raw score equal: the tie rule alone decides."""
+    W, L, C, kp = 16, 3000, 512, 5
+    lay = synth.make_inputs(5, [L, L + 7], 8, 2, 128, W, "bf16", nspans=2)
+    lay.q_win[:] = 0
+    gpu = parity.run_gpu(lay, kp, pool, C)
+    n, r = C - W, kp // 2
+    want = list(range(r, r + n)) if pool == "avg" else list(range(n))
+    for b in range(2):
+        for h in range(2):
+            assert gpu["idx"][b, h, :n].tolist() == want
+
+
+@pytest.mark.parametrize("name", ["1", "2"])
+def test_workload_full(name):
+    cfg = synth.CONFIGS[name]
+    lay = synth.make_layer(name)
+    _, gpu = _run_and_check(lay, cfg["k_pool"], cfg["pool"], cfg["C"])
+    _assert_planted(lay, gpu)
+
+
+def _assert_planted(lay, gpu):
+    for b in range(lay.B):
+        for h in range(lay.H_kv):
+            kept = set(gpu["idx"][b, h].tolist())
+            missing = [p for p in lay.targets[b][h] if p not in kept]
+            assert not missing, (b, h, missing[:8])
+
+
+@pytest.mark.parametrize("name,layer,seqs", [
+    ("3", 0, [0, 5]),
+    ("4", 0, [0]),
+    ("4", 31, [0]),
+    ("5a", 0, [7, 8]),     # the shortest and the longest prompt of the ragged batch
+    ("5b", 0, [0]),
+])
+def test_workload_full_size_sampled(name, layer, seqs):
+    cfg = synth.CONFIGS[name]
+    lay = synth.make_layer(name, layer)
+    gpu = parity.run_gpu(lay, cfg["k_pool"], cfg["pool"], cfg["C"])
+    _assert_planted(lay, gpu)
+    ora = parity.oracle_for(lay, cfg["k_pool"], cfg["pool"], cfg["C"], seqs=seqs)
+    parity.check(lay, gpu, ora, cfg["C"], seqs=seqs)
+
+
+def test_repeated_calls_reuse_workspace():
+    lay = synth.make_inputs(9, [5000, 2000], 32, 8, 128, 32, "bf16", nspans=4)
+    q, k, v = (parity.to_device(x) for x in (lay.q_win, lay.k, lay.v))
+    a = S.compress(q, k, v, lay.seqlens, 32, 7, "max", 1024)
+    b = S.compress(q, k, v, lay.seqlens, 32, 7, "max", 1024, workspace=a[3])
+    for x, y in zip(a[:3], b[:3]):
+        assert torch.equal(x, y)
+
+
+def test_host_buffer_entry_point_matches_device():
+    lay = synth.make_inputs(10, [4000, 700], 32, 8, 128, 32, "bf16", nspans=4)
+    C = 1024
+    gpu = parity.run_gpu(lay, 7, "avg", C)
+    q, k, v = (torch.from_numpy(x).view(torch.bfloat16).pin_memory()
+               for x in (lay.q_win, lay.k, lay.v))
+    B, H_kv, d = lay.B, lay.H_kv, lay.d
+    ok = torch.empty((B, C, H_kv, d), dtype=torch.bfloat16).pin_memory()
+    ov = torch.empty_like(ok)
+    oi = torch.empty((B, H_kv, C), dtype=torch.int32).pin_memory()
+    shape = S.make_shape(B, lay.H_q, H_kv, d, S.BF16)
+    staging = torch.empty(S.host_staging_size(shape, lay.seqlens, 32, C), dtype=torch.uint8,
+                          device="cuda")
+    S.compress_host(q, k, v, lay.seqlens, 32, 7, "avg", C, ok, ov, oi, staging)
+    np.testing.assert_array_equal(oi.numpy(), gpu["idx"])
+    np.testing.assert_array_equal(ok.view(torch.int16).numpy().view(np.uint16), gpu["out_k"])
+    np.testing.assert_array_equal(ov.view(torch.int16).numpy().view(np.uint16), gpu["out_v"])
+
+
+def test_argument_errors_enqueue_nothing():
+    lay = synth.make_inputs(11, [3000], 8, 2, 64, 16, "bf16", nspans=2)
+    q, k, v = (parity.to_device(x) for x in (lay.q_win, lay.k, lay.v))
+    with pytest.raises(S.SnapKVError) as e:
+        S.compress(q, k, v, lay.seqlens, 16, 4, "avg", 256)
+    assert e.value.code == S.ERR_INVALID_ARG
+    with pytest.raises(S.SnapKVError) as e:
+        S.compress(q, k, v, lay.seqlens, 16, 5, "avg", 256,
+                   workspace=torch.empty(64, dtype=torch.uint8, device="cuda"))
+    assert e.value.code == S.ERR_WORKSPACE
