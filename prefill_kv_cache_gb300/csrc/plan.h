@@ -15,6 +15,7 @@ constexpr int kMaxRows = 256;      // W * g limit (query rows per KV head)
 constexpr int kMaxBatch = 4096;
 constexpr int kClusterCTAs = 8;    // CTAs per (sequence, KV head) in select/gather
 constexpr int kSelectThreads = 512;
+constexpr int kCounterInts = 1024;  // work-queue counters in the workspace
 
 // Status word values written by kernels (0 = fine).
 constexpr int kDevOk = 0;
@@ -52,6 +53,9 @@ struct Plan {
   float2* stats;     // [total_pieces * Wp] (running max, sum of exp) per piece and row
   float* lse;        // [nseq * H_kv * Wp] natural-log LSE per (sequence, head, row)
   int* status;       // device status word
+  int* counters;     // work-queue head and per-group completion counters
+  long long total_rows;  // rows of k / v in the whole call (T)
+  int batch;         // sequences in the whole call (B)
   SeqInfo seq[kGroupSeqs];
 };
 

@@ -1,14 +1,766 @@
-// Tensor-core (tcgen05 / TMA) observation-window score kernel.  Placeholder
-// that declines every problem until the kernel lands; the caller then runs
-// the CUDA-core path.
+// Observation-window scores on the 5th-generation tensor cores (tcgen05),
+// bf16 inputs, head dim 64 or 128, W*g = 128 or 256 query rows per KV head.
+//
+// What it computes is the window attention score of every prefix key: the
+// softmax(q.k / sqrt(d)) probabilities of the last W prompt queries over
+// their causally visible keys, summed over those queries and averaged over
+// the query heads of the KV group (jisaku.com glossary "SnapKV",
+// "SnapKVの仕組み"; hotpaper.ai summary of "SnapKV: LLM Knows What You are
+// Looking for Before Generation", "핵심 아이디어").  The W x L probability
+// matrix is never stored: K is swept twice.
+//
+//   pass 1 (S = Q K^T, query rows on TMEM lanes): per key piece, each
+//     thread keeps the running max and sum of exp2 of one query row;
+//   merge: per row, the log2-sum-exp2 over the pieces of its KV head;
+//   pass 2 (S^T = K Q^T, keys on TMEM lanes): each thread sums
+//     exp2(logit * log2e / sqrt(d) - lse2) over all query rows of its key.
+//
+// Kernel shape: persistent, one CTA per SM, 10 warps:
+//   warp 0  TMA producer (K tiles of 128 keys, Q of the current KV head),
+//   warp 1  MMA issuer (single thread) and TMEM owner (512 columns),
+//   warps 2-9 two consumer warpgroups; warpgroup w reads TMEM buffer w, so
+//     the two groups take alternate key tiles.
+// Work items come from a device-wide queue in the order
+//   P1(0) | P1(1) M(0) P2(0) | P1(2) M(1) P2(1) | ... | M(G-1) P2(G-1)
+// where a group is ~1024 key tiles of whole KV heads, P1 / P2 are pass-1 /
+// pass-2 pieces of 8 tiles and M are merge items.  Pass 2 of a group
+// re-reads K that pass 1 streamed through L2 one group earlier.  A merge item
+// waits for its group's pass-1 pieces and a pass-2 item for its group's
+// merges; both always sit later in the queue than what they wait for, so
+// the waits cannot form a cycle whatever the number of resident CTAs.
+// Every wait is bounded: on expiry the kernel sets the status word to
+// "timeout", stops taking work, lets its own copies and MMAs drain, frees its
+// TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <cstdint>
+#include <cstring>
+
 #include "plan.h"
+#include "tmem_ld.cuh"
 
 namespace snapkv {
+namespace tc {
 
-int launch_score_tc(const Plan&, void*, bool* taken) {
+constexpr int kThreads = 320;
+constexpr int kConsumerThreads = 256;
+constexpr int kTileKeys = 128;
+constexpr int kTilesPerPiece = 8;  // 1024 keys, the piece size of the stats layout
+constexpr int kMaxStages = 8;
+constexpr int kRing = 4;
+constexpr int kMaxGroups = 128;
+constexpr int kGroupTiles = 1024;
+constexpr int kMergeRows = 32;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSmemLimit = 232448;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
+
+enum : int { kP1 = 0, kMerge = 1, kP2 = 2, kDone = 3 };
+
+struct Group {
+  int u0, u1;                       // units (seq * H_kv + head) [u0, u1)
+  int p1_items, m_items, p2_items;  // items of each kind
+  int p1_start, m_start, p2_start;  // their first queue index
+};
+
+struct TcPlan {
+  int ngroups, total_items, stages, wp;
+  int* counters;  // [0] queue head; [1+g] pass-1 pieces done; [1+G+g] merges done
+  Group grp[kMaxGroups];
+};
+
+struct Entry {
+  int type, g, u, piece, tile0, ntiles, row0, nrows;
+};
+
+// ------------------------------------------------------------ PTX layer ---
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
+                   smem_addr(b)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.b32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_addr(b)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+struct Ctl {
+  volatile int* abort;  // CTA-wide abort flag (shared memory)
+  int* status;          // device status word
+};
+
+__device__ __forceinline__ void raise_timeout(const Ctl& c) {
+  *c.abort = 1;
+  atomicExch(c.status, kDevTimeout);
+}
+
+// Bounded wait for the phase of parity `parity` of barrier b.  Returns false
+// when the CTA is aborting (flag already set, or this wait expired).
+__device__ __noinline__ bool wait_bar(uint64_t* b, uint32_t parity, const Ctl& c) {
+  if (mbar_test(b, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test(b, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*c.abort) return false;
+      if (global_ns() - t0 > kWaitNs) {
+        raise_timeout(c);
+        return false;
+      }
+    }
+  }
+}
+
+// Bounded wait until *ctr >= target (device-scope acquire).
+__device__ __noinline__ bool wait_counter(const int* ctr, int target, const Ctl& c) {
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if (*c.abort) return false;
+    if (global_ns() - t0 > kWaitNs) {
+      raise_timeout(c);
+      return false;
+    }
+    __nanosleep(128);
+  }
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
+// layout (rows of 64 bf16 = 128 B, 8-row atoms 1024 B apart).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address
+  d |= (uint64_t)1u << 16;                  // leading-dimension offset (unused here)
+  d |= (uint64_t)(1024u >> 4) << 32;        // stride between 8-row atoms
+  d |= (uint64_t)1u << 46;                  // descriptor version
+  d |= (uint64_t)2u << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* b) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(b))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ------------------------------------------------------------ schedule ---
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ Entry decode(const Plan& p, const TcPlan& tp, int idx) {
+  Entry e{};
+  e.type = kDone;
+  if (idx >= tp.total_items) return e;
+  for (int g = 0; g < tp.ngroups; ++g) {
+    const Group& G = tp.grp[g];
+    int kind = -1, local = 0;
+    if (idx >= G.p1_start && idx < G.p1_start + G.p1_items) {
+      kind = kP1;
+      local = idx - G.p1_start;
+    } else if (idx >= G.m_start && idx < G.m_start + G.m_items) {
+      kind = kMerge;
+      local = idx - G.m_start;
+    } else if (idx >= G.p2_start && idx < G.p2_start + G.p2_items) {
+      kind = kP2;
+      local = idx - G.p2_start;
+    }
+    if (kind < 0) continue;
+    e.type = kind;
+    e.g = g;
+    if (kind == kMerge) {
+      e.row0 = local * kMergeRows;
+      e.nrows = min(kMergeRows, (G.u1 - G.u0) * tp.wp - e.row0);
+      return e;
+    }
+    for (int u = G.u0; u < G.u1; ++u) {
+      const SeqInfo& S = p.seq[u / p.H_kv];
+      if (!S.scored) continue;
+      const int keys = kind == kP1 ? S.L : S.P;
+      const int tiles = ceil_div(keys, kTileKeys);
+      const int pieces = ceil_div(tiles, kTilesPerPiece);
+      if (local < pieces) {
+        e.u = u;
+        e.piece = local;
+        e.tile0 = local * kTilesPerPiece;
+        e.ntiles = min(kTilesPerPiece, tiles - e.tile0);
+        return e;
+      }
+      local -= pieces;
+    }
+    e.type = kDone;  // unreachable with a consistent plan
+    return e;
+  }
+  return e;
+}
+
+// ---------------------------------------------------------- the kernel ---
+
+__global__ void __launch_bounds__(kThreads, 1)
+score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan tp,
+                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NS = tp.stages, wp = tp.wp, d = p.d;
+  const int halves = d / 64;
+  const uint32_t q_half_bytes = (uint32_t)wp * 128u;
+  const uint32_t q_bytes = q_half_bytes * halves;
+  const uint32_t k_half_bytes = kTileKeys * 128u;
+  const uint32_t k_bytes = k_half_bytes * halves;
+
+  uint8_t* qbuf = smem;
+  uint8_t* kbuf = smem + 2 * q_bytes;
+  float* aux = reinterpret_cast<float*>(kbuf + (size_t)NS * k_bytes);  // 512 floats
+  uint64_t* bars = reinterpret_cast<uint64_t*>(aux + 512);
+  uint64_t* full = bars;
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* qfull = empty + kMaxStages;
+  uint64_t* qempty = qfull + 2;
+  uint64_t* tfull = qempty + 2;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* sfull = tempty + 2;
+  uint64_t* sempty = sfull + kRing;
+  uint64_t* cbar = sempty + kRing;  // consumer-group barrier (256 arrivals)
+  uint64_t* drain = cbar + 1;       // MMA drain at teardown
+  Entry* ring = reinterpret_cast<Entry*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ring + kRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(abort_flag) + 1);
+  const Ctl ctl{abort_flag, p.status};
+
+  if (threadIdx.x == 0) {
+    if ((smem_addr(smem) & 1023u) != 0) atomicExch(p.status, kDevTimeout);
+    for (int s = 0; s < kMaxStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&qfull[b], 1);
+      mbar_init(&qempty[b], 1);
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sempty[s], 9);  // MMA thread + 8 consumer warps
+    }
+    mbar_init(cbar, kConsumerThreads);
+    mbar_init(drain, 1);
+    *abort_flag = (smem_addr(smem) & 1023u) != 0 ? 1 : 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+            smem_addr(tmem_slot)),
+        "r"(kTmemCols)
+        : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const float c2 = p.log2e_scale;  // log2(e) / sqrt(d)
+
+  if (warp == 0) {
+    // ------------------------------------------------------ producer ---
+    if (lane == 0) {
+      int ring_n = 0, item_n = 0, stage_n = 0;
+      int fills[kMaxStages] = {0, 0, 0, 0, 0, 0, 0, 0};
+      int qfills[2] = {0, 0};
+      for (;;) {
+        const int idx = *abort_flag ? tp.total_items : atomicAdd(&tp.counters[0], 1);
+        const Entry e = decode(p, tp, idx);
+        const int slot = ring_n % kRing;
+        if (!wait_bar(&sempty[slot], ((ring_n / kRing) & 1) ^ 1, ctl)) break;
+        ring[slot] = e;
+        mbar_arrive(&sfull[slot]);
+        ++ring_n;
+        if (e.type == kDone) break;
+        if (e.type == kMerge) continue;
+        const SeqInfo& S = p.seq[e.u / p.H_kv];
+        const int h = e.u % p.H_kv;
+        const int qb = item_n & 1;
+        if (!wait_bar(&qempty[qb], ((item_n >> 1) & 1) ^ 1, ctl)) break;
+        mbar_arrive_tx(&qfull[qb], q_bytes);
+        for (int hf = 0; hf < halves; ++hf)
+          tma_load_3d(smem_addr(qbuf + qb * q_bytes + hf * q_half_bytes), &tm_q, &qfull[qb],
+                      hf * 64, h * p.g, S.b * p.W);
+        ++qfills[qb];
+        bool ok = true;
+        for (int t = 0; t < e.ntiles; ++t) {
+          const int st = stage_n % NS;
+          if (!wait_bar(&empty[st], ((stage_n / NS) & 1) ^ 1, ctl)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_tx(&full[st], k_bytes);
+          const int row = (int)S.row0 + (e.tile0 + t) * kTileKeys;
+          for (int hf = 0; hf < halves; ++hf)
+            tma_load_3d(smem_addr(kbuf + st * k_bytes + hf * k_half_bytes), &tm_k, &full[st],
+                        hf * 64, h, row);
+          ++fills[st];
+          ++stage_n;
+        }
+        ++item_n;
+        if (!ok) break;
+      }
+      // drain: every copy this thread issued lands before the CTA leaves
+      for (int s = 0; s < NS; ++s)
+        if (fills[s] > 0) {  // completion of the last fill of stage s
+          const uint64_t t0 = global_ns();
+          while (!mbar_test(&full[s], (uint32_t)((fills[s] - 1) & 1)) &&
+                 global_ns() - t0 < kWaitNs) {
+          }
+        }
+      for (int b = 0; b < 2; ++b)
+        if (qfills[b] > 0) {
+          const uint64_t t0 = global_ns();
+          while (!mbar_test(&qfull[b], (uint32_t)((qfills[b] - 1) & 1)) &&
+                 global_ns() - t0 < kWaitNs) {
+          }
+        }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA ---
+    if (lane == 0) {
+      int ring_n = 0, item_n = 0, stage_n = 0, tile_n = 0;
+      const uint32_t id_p1 = idesc_bf16(128, 128);
+      const uint32_t id_p2 = idesc_bf16(128, wp);
+      const int R = wp / 128;
+      bool issued = false;
+      for (;;) {
+        const int slot = ring_n % kRing;
+        if (!wait_bar(&sfull[slot], (ring_n / kRing) & 1, ctl)) break;
+        const Entry e = ring[slot];
+        ++ring_n;
+        mbar_arrive(&sempty[slot]);
+        if (e.type == kDone) break;
+        if (e.type == kMerge) continue;
+        const int qb = item_n & 1;
+        if (!wait_bar(&qfull[qb], (item_n >> 1) & 1, ctl)) break;
+        tc_fence_after();
+        const uint32_t qa = smem_addr(qbuf + qb * q_bytes);
+        bool ok = true;
+        for (int t = 0; t < e.ntiles; ++t) {
+          const int st = stage_n % NS;
+          const int ab = tile_n & 1;
+          if (!wait_bar(&full[st], (stage_n / NS) & 1, ctl) ||
+              !wait_bar(&tempty[ab], ((tile_n >> 1) & 1) ^ 1, ctl)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ka = smem_addr(kbuf + st * k_bytes);
+          const uint32_t dcol = tmem + (uint32_t)ab * 256u;
+          if (e.type == kP1) {
+            for (int rb = 0; rb < R; ++rb)
+              for (int kk = 0; kk < d / 16; ++kk) {
+                const uint64_t ad = sw128_desc(qa + (uint32_t)(kk >> 2) * q_half_bytes +
+                                               (uint32_t)rb * 128u * 128u + (uint32_t)(kk & 3) * 32u);
+                const uint64_t bd = sw128_desc(ka + (uint32_t)(kk >> 2) * k_half_bytes +
+                                               (uint32_t)(kk & 3) * 32u);
+                mma_bf16(dcol + (uint32_t)rb * 128u, ad, bd, id_p1, kk > 0);
+              }
+          } else {
+            for (int kk = 0; kk < d / 16; ++kk) {
+              const uint64_t ad = sw128_desc(ka + (uint32_t)(kk >> 2) * k_half_bytes +
+                                             (uint32_t)(kk & 3) * 32u);
+              const uint64_t bd = sw128_desc(qa + (uint32_t)(kk >> 2) * q_half_bytes +
+                                             (uint32_t)(kk & 3) * 32u);
+              mma_bf16(dcol, ad, bd, id_p2, kk > 0);
+            }
+          }
+          mma_commit(&empty[st]);
+          mma_commit(&tfull[ab]);
+          issued = true;
+          ++stage_n;
+          ++tile_n;
+        }
+        mma_commit(&qempty[qb]);
+        ++item_n;
+        if (!ok) break;
+      }
+      if (issued) {
+        // all MMAs this thread issued have completed once `drain` flips
+        mma_commit(drain);
+        const uint64_t t0 = global_ns();
+        while (!mbar_test(drain, 0) && global_ns() - t0 < kWaitNs) {
+        }
+      }
+    }
+  } else {
+    // ----------------------------------------------------- consumers ---
+    const int ct = threadIdx.x - 64;          // 0..255
+    const int wg = ct >> 7;                   // warpgroup: TMEM buffer it reads
+    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+    const int lrow = quarter * 32 + lane;     // TMEM lane of this thread
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const int R = wp / 128;
+    int ring_n = 0, tile_n = 0;
+    uint32_t cphase = 0;
+    auto csync = [&]() -> bool {  // all 256 consumer threads
+      mbar_arrive(cbar);
+      const bool r = wait_bar(cbar, cphase, ctl);
+      cphase ^= 1;
+      return r;
+    };
+    float s[kTileKeys];
+    for (;;) {
+      const int slot = ring_n % kRing;
+      if (!wait_bar(&sfull[slot], (ring_n / kRing) & 1, ctl)) break;
+      const Entry e = ring[slot];
+      ++ring_n;
+      if (e.type == kDone) break;
+      if (!csync()) break;  // previous item fully finished by both groups
+      const Group& G = tp.grp[e.g];
+      if (e.type == kMerge) {
+        if (ct == 0) wait_counter(&tp.counters[1 + e.g], G.p1_items, ctl);
+        if (!csync() || *abort_flag) break;
+        // 8 threads per row, pieces strided over them
+        const int rl = ct >> 3, sub = ct & 7;
+        const int gr = e.row0 + rl;
+        float M = -INFINITY, Z = 0.f;
+        int u = -1, r = 0;
+        if (rl < e.nrows) {
+          u = G.u0 + gr / wp;
+          r = gr % wp;
+          const SeqInfo& S = p.seq[u / p.H_kv];
+          if (S.scored) {
+            const int h = u % p.H_kv;
+            const float2* st = p.stats + (size_t)(S.piece0 + h * S.chunks) * wp + r;
+            for (int c = sub; c < S.chunks; c += 8) {
+              const float2 v = __ldcg(st + (size_t)c * wp);
+              if (v.x == -INFINITY) continue;
+              if (v.x > M) {
+                Z = Z * exp2f(M - v.x) + v.y;
+                M = v.x;
+              } else {
+                Z += v.y * exp2f(v.x - M);
+              }
+            }
+          } else {
+            u = -1;
+          }
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+          const float Mo = __shfl_xor_sync(0xffffffffu, M, o);
+          const float Zo = __shfl_xor_sync(0xffffffffu, Z, o);
+          const float Mn = fmaxf(M, Mo);
+          if (Mn != -INFINITY) Z = Z * exp2f(M - Mn) + Zo * exp2f(Mo - Mn);
+          M = Mn;
+        }
+        if (sub == 0 && u >= 0) p.lse[(size_t)u * wp + r] = M + log2f(Z);
+        __threadfence();
+        if (!csync()) break;
+        if (ct == 0) atomicAdd(&tp.counters[1 + tp.ngroups + e.g], 1);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sempty[slot]);
+        continue;
+      }
+
+      const int s_idx = e.u / p.H_kv, h = e.u % p.H_kv;
+      const SeqInfo& S = p.seq[s_idx];
+      bool ok = true;
+      if (e.type == kP2) {
+        if (ct == 0) wait_counter(&tp.counters[1 + tp.ngroups + e.g], G.m_items, ctl);
+        if (!csync() || *abort_flag) break;
+        for (int r = ct; r < wp; r += kConsumerThreads) aux[r] = __ldcg(p.lse + (size_t)e.u * wp + r);
+        if (!csync()) break;
+      }
+      // pass-1 running statistics of this thread's rows (R row blocks)
+      float Mrow[2] = {-INFINITY, -INFINITY}, Zrow[2] = {0.f, 0.f};
+      float* raw_out = p.raw + S.score0 + (size_t)h * S.P;
+      const float inv_g = 1.0f / (float)p.g;
+      for (int t = 0; t < e.ntiles; ++t, ++tile_n) {
+        if ((tile_n & 1) != wg) continue;
+        if (!wait_bar(&tfull[wg], (tile_n >> 1) & 1, ctl)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int key0 = (e.tile0 + t) * kTileKeys;
+        const uint32_t tb = tmem + lane_addr + (uint32_t)wg * 256u;
+        if (e.type == kP1) {
+          for (int rb = 0; rb < R; ++rb) {
+            const int row = rb * 128 + lrow;
+            const int limit = min(S.P + row / p.g, S.L - 1);  // last visible key
+            __syncwarp();  // tcgen05.ld is warp-collective
+            tmem_load64(tb + (uint32_t)rb * 128u, s);
+            tmem_load64(tb + (uint32_t)rb * 128u + 64u, s + 64);
+            float tmax = -INFINITY;
+            if (key0 + kTileKeys - 1 <= limit) {
+#pragma unroll
+              for (int j = 0; j < kTileKeys; ++j) tmax = fmaxf(tmax, s[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < kTileKeys; ++j) {
+                if (key0 + j > limit) s[j] = -INFINITY;
+                tmax = fmaxf(tmax, s[j]);
+              }
+            }
+            if (tmax != -INFINITY) {  // some key of this tile is visible to the row
+              const float Mn = fmaxf(Mrow[rb], tmax * c2);
+              float z = Zrow[rb] * ex2(Mrow[rb] - Mn);
+              float z1 = 0.f, z2 = 0.f, z3 = 0.f;
+#pragma unroll
+              for (int j = 0; j < kTileKeys; j += 4) {
+                z += ex2(fmaf(s[j], c2, -Mn));
+                z1 += ex2(fmaf(s[j + 1], c2, -Mn));
+                z2 += ex2(fmaf(s[j + 2], c2, -Mn));
+                z3 += ex2(fmaf(s[j + 3], c2, -Mn));
+              }
+              Zrow[rb] = (z + z1) + (z2 + z3);
+              Mrow[rb] = Mn;
+            }
+          }
+        } else {
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          for (int c0 = 0; c0 < wp; c0 += 64) {
+            __syncwarp();
+            tmem_load64(tb + (uint32_t)c0, s);
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+              const float4 m4 = *reinterpret_cast<const float4*>(aux + c0 + j);
+              a0 += ex2(fmaf(s[j], c2, -m4.x));
+              a1 += ex2(fmaf(s[j + 1], c2, -m4.y));
+              a2 += ex2(fmaf(s[j + 2], c2, -m4.z));
+              a3 += ex2(fmaf(s[j + 3], c2, -m4.w));
+            }
+          }
+          const int key = key0 + lrow;
+          if (key < S.P) raw_out[key] = ((a0 + a1) + (a2 + a3)) * inv_g;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[wg]);
+      }
+      if (!ok) break;
+      if (e.type == kP1) {
+        // merge the two groups' statistics of each row, then publish
+        float2* comb = reinterpret_cast<float2*>(aux);
+        if (wg == 1)
+          for (int rb = 0; rb < R; ++rb) comb[rb * 128 + lrow] = make_float2(Mrow[rb], Zrow[rb]);
+        if (!csync()) break;
+        if (wg == 0) {
+          const size_t piece = (size_t)S.piece0 + (size_t)h * S.chunks + e.piece;
+          for (int rb = 0; rb < R; ++rb) {
+            const float2 o = comb[rb * 128 + lrow];
+            float M = Mrow[rb], Z = Zrow[rb];
+            const float Mn = fmaxf(M, o.x);
+            if (Mn != -INFINITY) Z = Z * ex2(M - Mn) + o.y * ex2(o.x - Mn);
+            p.stats[piece * wp + rb * 128 + lrow] = make_float2(Mn, Z);
+          }
+          __threadfence();
+        }
+        if (!csync()) break;
+        if (ct == 0) atomicAdd(&tp.counters[1 + e.g], 1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[slot]);
+    }
+  }
+
+  // ---------------------------------------------------------- teardown ---
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                 : "memory");
+}
+
+// --------------------------------------------------------------- host ---
+
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiled get_encoder() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(ptr);
+  }
+  return fn;
+}
+
+// 3-D bf16 tensor map {d, heads, rows}, box {64, box1, box2}, 128 B swizzle.
+bool make_map(CUtensorMap* m, const void* base, int d, int heads, long long rows, int box1,
+              int box2) {
+  EncodeTiled enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)d * 2 * heads};
+  cuuint32_t box[3] = {64, (cuuint32_t)box1, (cuuint32_t)box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+// Builds the item queue for one launch group and launches the kernel, or
+// declines (taken = false) for shapes it does not cover.
+int launch_score_tc(const Plan& p, void* stream, bool* taken) {
+  using namespace tc;
   *taken = false;
+  if (p.dtype != 0 || (p.d != 64 && p.d != 128) || (p.Wp != 128 && p.Wp != 256)) return cudaSuccess;
+  if (p.chunk_keys != kTileKeys * kTilesPerPiece || p.counters == nullptr) return cudaSuccess;
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) return cudaErrorUnknown;
+  }
+  TcPlan tp;
+  std::memset(&tp, 0, sizeof tp);
+  tp.wp = p.Wp;
+  tp.counters = p.counters;
+  // groups of whole KV heads, ~kGroupTiles key tiles each
+  const int units = p.nseq * p.H_kv;
+  int g = 0, acc = 0, u0 = 0;
+  for (int u = 0; u < units; ++u) {
+    const SeqInfo& S = p.seq[u / p.H_kv];
+    if (S.scored) acc += (S.L + kTileKeys - 1) / kTileKeys;
+    const bool last = u == units - 1;
+    if (acc >= kGroupTiles || (last && acc > 0)) {
+      if (g == kMaxGroups) return cudaSuccess;  // too many groups: leave it to the other path
+      tp.grp[g].u0 = u0;
+      tp.grp[g].u1 = u + 1;
+      ++g;
+      u0 = u + 1;
+      acc = 0;
+    }
+  }
+  tp.ngroups = g;
+  if (g == 0) return cudaSuccess;
+  for (int i = 0; i < g; ++i) {
+    Group& G = tp.grp[i];
+    for (int u = G.u0; u < G.u1; ++u) {
+      const SeqInfo& S = p.seq[u / p.H_kv];
+      if (!S.scored) continue;
+      const int t1 = (S.L + kTileKeys - 1) / kTileKeys, t2 = (S.P + kTileKeys - 1) / kTileKeys;
+      G.p1_items += (t1 + kTilesPerPiece - 1) / kTilesPerPiece;
+      G.p2_items += (t2 + kTilesPerPiece - 1) / kTilesPerPiece;
+    }
+    G.m_items = ((G.u1 - G.u0) * p.Wp + kMergeRows - 1) / kMergeRows;
+  }
+  // queue order: P1(0) | P1(1) M(0) P2(0) | ... | M(G-1) P2(G-1)
+  int idx = 0;
+  for (int k = 0; k <= g; ++k) {
+    if (k < g) {
+      tp.grp[k].p1_start = idx;
+      idx += tp.grp[k].p1_items;
+    }
+    if (k >= 1) {
+      tp.grp[k - 1].m_start = idx;
+      idx += tp.grp[k - 1].m_items;
+      tp.grp[k - 1].p2_start = idx;
+      idx += tp.grp[k - 1].p2_items;
+    }
+  }
+  tp.total_items = idx;
+
+  const uint32_t halves = p.d / 64;
+  const uint32_t q_bytes = (uint32_t)p.Wp * 128u * halves;
+  const uint32_t k_bytes = (uint32_t)kTileKeys * 128u * halves;
+  const uint32_t misc = 512 * 4 + (2 * kMaxStages + 8 + 2 * kRing + 2) * 8 + kRing * sizeof(Entry) + 8;
+  const long long room = (long long)kSmemLimit - 2 * (long long)q_bytes - misc;
+  int stages = (int)(room / k_bytes);
+  if (stages > 6) stages = 6;
+  if (stages < 2) return cudaSuccess;
+  tp.stages = stages;
+  const size_t smem = 2 * (size_t)q_bytes + (size_t)stages * k_bytes + misc;
+
+  if (p.g > 256 || p.W > 256) return cudaSuccess;
+  // the K map covers the rows of the whole call (rows past the end read as zeros)
+  CUtensorMap tm_k, tm_q;
+  if (!make_map(&tm_k, p.k, p.d, p.H_kv, p.total_rows, 1, kTileKeys)) return cudaSuccess;
+  if (!make_map(&tm_q, p.q, p.d, p.H_q, (long long)p.batch * p.W, p.g, p.W)) return cudaSuccess;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  // zero the queue head and the per-group counters
+  e = cudaMemsetAsync(p.counters, 0, sizeof(int) * (1 + 2 * g), st);
+  if (e != cudaSuccess) return e;
+  const int grid = sms < tp.total_items ? sms : tp.total_items;
+  score_tc_kernel<<<grid, kThreads, smem, st>>>(p, tp, tm_k, tm_q);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  count_launches(1);
+  *taken = true;
   return cudaSuccess;
 }
 

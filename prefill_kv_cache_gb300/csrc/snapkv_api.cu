@@ -28,6 +28,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Layout {
   size_t status = 0;  // int status word
+  size_t counters = 0;  // kCounterInts ints
   size_t raw = 0, pooled = 0, stats = 0, lse = 0;
   size_t score_count = 0;  // floats in raw (and in pooled)
   size_t total = 0;
@@ -72,6 +73,8 @@ Layout layout_for(const snapkv_shape* sh, const int32_t* seqlens, int W, int C) 
   size_t off = 0;
   lay.status = off;
   off += kAlign;
+  lay.counters = off;
+  off = align_up(off + kCounterInts * sizeof(int));
   lay.raw = off;
   off = align_up(off + scores * sizeof(float));
   lay.pooled = off;
@@ -182,6 +185,10 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
   p.stats = reinterpret_cast<float2*>(ws + lay.stats);
   p.lse = reinterpret_cast<float*>(ws + lay.lse);
   p.status = reinterpret_cast<int*>(ws + lay.status);
+  p.counters = reinterpret_cast<int*>(ws + lay.counters);
+  p.batch = shape->batch;
+  p.total_rows = 0;
+  for (int b = 0; b < shape->batch; ++b) p.total_rows += seqlens_host[b];
 
   long long row0 = 0, score0 = 0;
   for (int g0 = 0; g0 < shape->batch; g0 += kGroupSeqs) {

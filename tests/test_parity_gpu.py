@@ -129,3 +129,23 @@ def test_argument_errors_enqueue_nothing():
         S.compress(q, k, v, lay.seqlens, 16, 5, "avg", 256,
                    workspace=torch.empty(64, dtype=torch.uint8, device="cuda"))
     assert e.value.code == S.ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("H_q,H_kv,d,W,dtype,tc", [
+    (32, 8, 128, 32, "bf16", True),    # W*g = 128: tensor cores
+    (32, 8, 128, 64, "bf16", True),    # W*g = 256: tensor cores
+    (16, 8, 64, 64, "bf16", True),     # d = 64
+    (4, 4, 64, 16, "fp32", False),     # fp32 stays on CUDA cores
+    (8, 8, 128, 16, "bf16", False),    # W*g = 16: CUDA cores
+])
+def test_score_path_selection(H_q, H_kv, d, W, dtype, tc):
+    """bf16 with W*g in {128, 256} runs the single tcgen05 kernel; else 3 CUDA-core kernels."""
+    lay = synth.make_inputs(12, [3000], H_q, H_kv, d, W, dtype, nspans=2)
+    q, k = parity.to_device(lay.q_win), parity.to_device(lay.k)
+    shape = S.make_shape(1, H_q, H_kv, d, q.dtype)
+    ws = torch.empty(S.workspace_size(shape, [3000], W, 512), dtype=torch.uint8, device="cuda")
+    n0 = S.kernel_launches()
+    S.score(q, k, [3000], W, 512, ws)
+    torch.cuda.synchronize()
+    assert S.kernel_launches() - n0 == (1 if tc else 3)
+    assert S.get_status(ws) == S.OK
