@@ -179,6 +179,33 @@ int snapkv_compress_host(const snapkv_shape *shape, const void *q_win_host,
  */
 uint64_t snapkv_kernel_launches(void);
 
+/*
+ * snapkv_compress without a caller-provided workspace.  The SnapKV pages have
+ * no counterpart to this entry point; it exists for callers that cannot call
+ * cudaMalloc -- for example a plugin inside a serving engine whose device
+ * memory is all owned by the engine's own pool, or a latency-critical path
+ * that cannot afford cudaMalloc's implicit device-wide synchronisation.
+ *
+ * Arguments, outputs and results are exactly those of snapkv_compress; the
+ * caller still provides q_win, k, v and the three output buffers.  The
+ * scratch comes from a 16 MiB array built into the library's device image,
+ * which every GPU that loads the library keeps until the process exits.
+ * Problems whose snapkv_workspace_size exceeds 16 MiB are rejected with
+ * SNAPKV_ERR_WORKSPACE before anything is enqueued (one Llama-3-8B-shaped
+ * layer of 131072 tokens needs about 10.5 MB).  The call allocates nothing.
+ *
+ * The first call on a device looks up the array's device address (a CUDA
+ * runtime query, made once per device with that device current); make that
+ * first call before any stream capture.  All calls share the one array and
+ * it keeps the last call's contents: calls that may overlap on the GPU (other
+ * streams, other host threads) race on it and must be serialised by the
+ * caller.  snapkv_get_status does not apply to this entry point.
+ */
+int snapkv_compress_noalloc(const snapkv_shape *shape, const void *q_win, const void *k,
+                            const void *v, const int32_t *seqlens_host, int32_t W,
+                            int32_t kernel_size, int32_t pool_type, int32_t C, void *out_k,
+                            void *out_v, int32_t *out_idx, void *stream);
+
 /* Static text for a status code. */
 const char *snapkv_status_string(int status);
 

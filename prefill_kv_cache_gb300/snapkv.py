@@ -31,6 +31,7 @@ EXPORTED = (
     "snapkv_get_status",
     "snapkv_host_staging_size",
     "snapkv_compress_host",
+    "snapkv_compress_noalloc",
     "snapkv_kernel_launches",
     "snapkv_status_string",
     "snapkv_version",
@@ -80,6 +81,9 @@ def load() -> ctypes.CDLL:
     lib.snapkv_compress_host.argtypes = [shp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                          vp, sz, vp]
     lib.snapkv_compress_host.restype = ctypes.c_int
+    lib.snapkv_compress_noalloc.argtypes = [shp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
+                                            vp]
+    lib.snapkv_compress_noalloc.restype = ctypes.c_int
     lib.snapkv_status_string.argtypes = [ctypes.c_int]
     lib.snapkv_status_string.restype = ctypes.c_char_p
     lib.snapkv_version.argtypes = []
@@ -253,3 +257,24 @@ def compress_host(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seqlens
                                      _stream_handle(stream))
     if rc:
         raise SnapKVError(rc, "snapkv_compress_host")
+
+
+def compress_noalloc(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seqlens,
+                     window_size: int, kernel_size: int, pooling, max_capacity_prompt: int,
+                     out_k: torch.Tensor, out_v: torch.Tensor, out_idx: torch.Tensor,
+                     stream=None) -> None:
+    """snapkv_compress_noalloc (include/snapkv.h): no workspace argument.
+
+    For callers that cannot allocate device memory; the library's built-in
+    16 MiB scratch serves as workspace.  All buffers are the caller's.
+    """
+    B, W, H_q, d = q_win.shape
+    shape = make_shape(B, H_q, k.shape[1], d, q_win.dtype)
+    arr, _ = _seqlens_array(seqlens)
+    rc = load().snapkv_compress_noalloc(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(),
+                                        v.data_ptr(), arr, W, int(kernel_size),
+                                        pool_code(pooling), int(max_capacity_prompt),
+                                        out_k.data_ptr(), out_v.data_ptr(), out_idx.data_ptr(),
+                                        _stream_handle(stream))
+    if rc:
+        raise SnapKVError(rc, "snapkv_compress_noalloc")
