@@ -35,6 +35,10 @@ SMALL = [
     ([6000],                 32,   4, 128, 32, 2048, 9, "avg", "bf16"),  # W*g = 256
     ([1500],                  2,   1, 128, 64, 600, 11, "max", "fp32"),
     ([33, 17, 1],             4,   2, 64, 16, 40,   5, "avg", "bf16"),   # all keep-all
+    # W*g = 256 with fewer work items than SMs and partly masked last tiles
+    ([5000],                 32,   8, 128, 64, 1024, 13, "avg", "bf16"),
+    ([8192, 700, 3100],      32,   8, 128, 64, 1024, 5, "max", "bf16"),
+    ([2049],                 16,   4, 64, 64, 512,  7, "avg", "bf16"),
 ]
 
 
