@@ -1,16 +1,22 @@
 // Pooling, top-(C-W) selection and emission of the compressed cache.
 //
-// One thread-block cluster of kClusterCTAs CTAs handles one (sequence, KV
-// head).  The CTAs split the prefix [0, P) into contiguous slices and:
+// One thread-block cluster handles one (sequence, KV head).  Its size is a
+// power of two chosen per launch: large enough that all units together fill
+// the GPU and that each CTA's slice fits its shared-memory staging, at most 16
+// (8 where the GPU does not allow non-portable cluster sizes).  The CTAs split
+// the prefix [0, P) into contiguous slices and:
 //
 //   1. pool the raw scores of their slice (stride 1, k//2 zeros of padding,
 //      average divides by k, or maximum) -- jisaku.com glossary "SnapKV",
 //      "Pooling for Robustness"; hotpaper.ai summary of "SnapKV: LLM Knows
-//      What You are Looking for Before Generation", "기술적 접근법";
+//      What You are Looking for Before Generation", "기술적 접근법".  The
+//      raw scores are staged in shared memory tile by tile, the pooled slice
+//      stays there for the next steps;
 //   2. find the exact n-th largest pooled value T by a three-digit radix
 //      select over the fp32 bit patterns (scores are >= 0, so the unsigned
-//      patterns order like the values); per-digit histograms are merged
-//      through distributed shared memory;
+//      patterns order like the values).  Per-digit histograms are summed
+//      across the cluster through distributed shared memory: each CTA
+//      reduces a share of the bins, then every CTA reads the reduced bins;
 //   3. keep every position with a value above T and the lowest-positioned
 //      `need` positions equal to T (ties go to the lower position), in
 //      ascending order, via per-CTA counts and block prefix scans -- no sort;
@@ -30,7 +36,12 @@ namespace cg = cooperative_groups;
 namespace snapkv {
 
 constexpr int kWarps = kSelectThreads / 32;
-static_assert(kMaxRows < kSelectThreads, "window rows are copied in one pass");
+constexpr int kPer = 4;                        // consecutive positions per thread per pass
+constexpr int kChunk = kSelectThreads * kPer;  // positions per compaction pass
+constexpr int kMaxCluster = 16;
+constexpr int kPoolTile = 4096;                // raw scores staged per pooling step
+constexpr int kStageFloats = 44 * 1024;         // dynamic shared memory, in floats
+static_assert(kMaxRows < kChunk, "window rows are copied in one pass");
 
 __device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -54,55 +65,55 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
   return before + x - v;
 }
 
-__device__ __forceinline__ int block_flag_scan(bool f, int* wsum, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const unsigned bal = __ballot_sync(0xffffffffu, f);
-  if (lane == 0) wsum[warp] = __popc(bal);
-  __syncthreads();
-  int before = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const int s = wsum[w];
-    if (w < warp) before += s;
-    tot += s;
-  }
-  __syncthreads();
-  *total = tot;
-  return before + __popc(bal & ((1u << lane) - 1u));
-}
-
 // Copy `cnt` rows: source position pos[i] of the sequence -> output slot
-// slot0 + i (or slot = position when slot0 < 0), K and V, 16 B per access.
+// slot0 + i, K and V, 16 B per access.
 __device__ __forceinline__ void copy_rows(const Plan& p, const SeqInfo& S, int h,
                                           const int* pos, int cnt, int slot0, int vecs) {
   const uint4* kin = static_cast<const uint4*>(p.k);
   const uint4* vin = static_cast<const uint4*>(p.v);
   uint4* kout = static_cast<uint4*>(p.out_k);
   uint4* vout = static_cast<uint4*>(p.out_v);
-  for (int e = threadIdx.x; e < cnt * vecs; e += blockDim.x) {
-    const int it = e / vecs, vv = e % vecs;
-    const int src_pos = pos[it];
-    const int slot = slot0 < 0 ? src_pos : slot0 + it;
-    const size_t src = ((size_t)(S.row0 + src_pos) * p.H_kv + h) * vecs + vv;
-    const size_t dst = (((size_t)S.b * p.C + slot) * p.H_kv + h) * vecs + vv;
-    kout[dst] = __ldcs(kin + src);
-    vout[dst] = __ldcs(vin + src);
+  // kU independent 16-byte loads of K and of V in flight per thread
+  constexpr int kU = 4;
+  const int total = cnt * vecs;
+  for (int e0 = threadIdx.x; e0 < total; e0 += kU * blockDim.x) {
+    uint4 kv[kU], vv_[kU];
+    size_t dst[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int e = e0 + u * blockDim.x;
+      if (e < total) {
+        const int it = e / vecs, vv = e % vecs;
+        const size_t src = ((size_t)(S.row0 + pos[it]) * p.H_kv + h) * vecs + vv;
+        dst[u] = (((size_t)S.b * p.C + slot0 + it) * p.H_kv + h) * vecs + vv;
+        kv[u] = __ldcs(kin + src);
+        vv_[u] = __ldcs(vin + src);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (e0 + u * blockDim.x < total) {
+        kout[dst[u]] = kv[u];
+        vout[dst[u]] = vv_[u];
+      }
+    }
   }
 }
 
-__global__ void __cluster_dims__(kClusterCTAs, 1, 1) __launch_bounds__(kSelectThreads, 1)
-select_gather(const __grid_constant__ Plan p, int cache_floats) {
-  extern __shared__ __align__(16) float cache[];
-  __shared__ unsigned hist[2048];
-  __shared__ unsigned merged[2048];
+__global__ void __launch_bounds__(kSelectThreads, 2)
+select_gather(const __grid_constant__ Plan p, int cap_floats) {
+  extern __shared__ __align__(16) float dyn[];  // [raw staging tile + halo][pooled slice]
+  __shared__ unsigned hist[2048];                // this CTA's digit histogram
+  __shared__ unsigned mrg[2048];                 // cluster sums of the bins this CTA owns
+  __shared__ unsigned merged[2048];              // cluster sums of all bins
   __shared__ int wsum[kWarps];
-  __shared__ int sel_pos[kSelectThreads];
+  __shared__ int sel_pos[kChunk];
   __shared__ int sh_digit, sh_above;
   __shared__ int sh_cnt[2];
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
-  const int CS = kClusterCTAs;
+  const int CS = (int)cluster.num_blocks();
   const int t = threadIdx.x;
   const int unit = blockIdx.y;
   const int s = unit / p.H_kv, h = unit % p.H_kv;
@@ -137,46 +148,96 @@ select_gather(const __grid_constant__ Plan p, int cache_floats) {
   const int P = S.P, n = p.n, r = p.kp / 2;
   const int Sz = (P + CS - 1) / CS;
   const int j0 = min(P, rank * Sz), j1 = min(P, j0 + Sz);
-  const int cnt_local = j1 - j0;
-  const bool use_cache = cnt_local <= cache_floats;
+  const int cnt = j1 - j0;
   const float* raw = p.raw + S.score0 + (size_t)h * P;
   float* pooled = p.pooled + S.score0 + (size_t)h * P;
+  const bool in_smem = kPoolTile + 2 * r + cnt <= cap_floats;
+  float* sraw = dyn;
+  float* spool = dyn + kPoolTile + 2 * r;
 
-  // 1. pooling of this CTA's slice
-  for (int j = j0 + t; j < j1; j += blockDim.x) {
-    float acc = 0.f, mx = -INFINITY;
-    for (int tt = j - r; tt <= j + r; ++tt) {
-      const float x = (tt >= 0 && tt < P) ? __ldcg(raw + tt) : 0.f;
-      acc += x;
-      mx = fmaxf(mx, x);
+  // 1. pooling of this CTA's slice (zero padding outside [0, P)), the raw
+  //    scores staged in shared memory one tile (plus halo) at a time
+  if (in_smem) {
+    for (int x0 = 0; x0 < cnt; x0 += kPoolTile) {
+      const int m = min(kPoolTile, cnt - x0);
+      for (int x1 = t; x1 < m + 2 * r; x1 += 4 * blockDim.x) {  // 4 loads in flight
+        float v4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int x = x1 + u * blockDim.x;
+          const int jj = j0 + x0 - r + x;
+          v4[u] = (x < m + 2 * r && jj >= 0 && jj < P) ? __ldcg(raw + jj) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (x1 + u * blockDim.x < m + 2 * r) sraw[x1 + u * blockDim.x] = v4[u];
+      }
+      __syncthreads();
+      for (int x = t; x < m; x += blockDim.x) {
+        float acc = 0.f, mx = -INFINITY;
+        for (int q = 0; q <= 2 * r; ++q) {
+          const float v = sraw[x + q];
+          acc += v;
+          mx = fmaxf(mx, v);
+        }
+        const float v = p.pool == 0 ? acc / (float)p.kp : mx;
+        spool[x0 + x] = v;
+        pooled[j0 + x0 + x] = v;
+      }
+      __syncthreads();
     }
-    const float v = p.pool == 0 ? acc / (float)p.kp : mx;
-    pooled[j] = v;
-    if (use_cache) cache[j - j0] = v;
+  } else {
+    for (int j = j0 + t; j < j1; j += blockDim.x) {
+      float acc = 0.f, mx = -INFINITY;
+      for (int tt = j - r; tt <= j + r; ++tt) {
+        const float v = (tt >= 0 && tt < P) ? __ldcg(raw + tt) : 0.f;
+        acc += v;
+        mx = fmaxf(mx, v);
+      }
+      pooled[j] = p.pool == 0 ? acc / (float)p.kp : mx;
+    }
   }
   __syncthreads();
-  const float* vals = use_cache ? cache : pooled + j0;
+  const float* vals = in_smem ? spool : pooled + j0;  // this CTA's pooled slice
 
   if (n > 0) {
-    // 2. radix select of the n-th largest value (digits 11/11/10 bits)
+    // 2. radix select of the n-th largest value (digits of 11, 11 and 10 bits)
     unsigned prefix = 0, mask = 0;
     int need = n;
     for (int pass = 0; pass < 3; ++pass) {
       const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
       const int nb = pass == 2 ? 1024 : 2048;
+      const int own = nb / CS;  // bins reduced by each CTA
       for (int b = t; b < 2048; b += blockDim.x) hist[b] = 0;
       __syncthreads();
-      for (int j = t; j < cnt_local; j += blockDim.x) {
-        const unsigned u = __float_as_uint(use_cache ? vals[j] : __ldcg(vals + j));
+      for (int x = t; x < cnt; x += blockDim.x) {
+        const unsigned u = __float_as_uint(vals[x]);
         if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
       }
       cluster.sync();
-      for (int b = t; b < nb; b += blockDim.x) {
+      for (int b = rank * own + t; b < (rank + 1) * own; b += blockDim.x) {
+        unsigned part[kMaxCluster];  // independent remote loads
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q)
+          part[q] = q < CS ? cluster.map_shared_rank(hist, q)[b] : 0u;
         unsigned sum = 0;
-        for (int q = 0; q < CS; ++q) sum += cluster.map_shared_rank(hist, q)[b];
-        merged[b] = sum;
+#pragma unroll
+        for (int q = 0; q < kMaxCluster; ++q) sum += part[q];
+        mrg[b] = sum;
       }
       cluster.sync();
+      for (int b1 = t; b1 < nb; b1 += 4 * blockDim.x) {
+        unsigned m4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int b = b1 + u * blockDim.x;
+          m4[u] = b < nb ? cluster.map_shared_rank(mrg, b / own)[b] : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (b1 + u * blockDim.x < nb) merged[b1 + u * blockDim.x] = m4[u];
+      }
+      __syncthreads();
       // digit D with count(> D) < need <= count(>= D); bins scanned from the top
       int local[4], lsum = 0;
 #pragma unroll
@@ -209,8 +270,8 @@ select_gather(const __grid_constant__ Plan p, int cache_floats) {
 
     // 3. per-CTA counts above / equal to T, exchanged across the cluster
     int my_gt = 0, my_eq = 0;
-    for (int j = t; j < cnt_local; j += blockDim.x) {
-      const unsigned u = __float_as_uint(use_cache ? vals[j] : __ldcg(vals + j));
+    for (int x = t; x < cnt; x += blockDim.x) {
+      const unsigned u = __float_as_uint(vals[x]);
       my_gt += u > T;
       my_eq += u == T;
     }
@@ -233,25 +294,45 @@ select_gather(const __grid_constant__ Plan p, int cache_floats) {
       }
       eq_acc += e_;
     }
-    cluster.sync();  // nobody leaves while others still read its counts
+    cluster.sync();  // nobody leaves while others still read its shared memory
 
-    // ascending compaction of the slice, chunk by chunk, with the row copies
+    // 4. ascending compaction of the slice, kPer consecutive positions per
+    //    thread per pass, with the row copies
     int running = 0;
-    for (int base = 0; base < cnt_local; base += blockDim.x) {
-      const int jj = base + t;
-      const bool in = jj < cnt_local;
-      const unsigned u = in ? __float_as_uint(use_cache ? vals[jj] : __ldcg(vals + jj)) : 0u;
-      const bool gt = in && u > T;
-      const bool eq = in && u == T;
+    for (int base = 0; base < cnt; base += kChunk) {
+      const int x0 = base + t * kPer;
+      bool gt[kPer], eq[kPer];
+      int n_eq = 0;
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const bool in = x0 + q < cnt;
+        const unsigned u = in ? __float_as_uint(vals[x0 + q]) : 0u;
+        gt[q] = in && u > T;
+        eq[q] = in && u == T;
+        n_eq += eq[q];
+      }
       int chunk_eq, chunk_sel;
-      const int eq_rank = block_flag_scan(eq, wsum, &chunk_eq);
-      const bool sel = gt || (eq && eq_before + eq_rank < need);
-      const int pos = block_flag_scan(sel, wsum, &chunk_sel);
+      int eq_rank = eq_before + block_excl_scan(n_eq, wsum, &chunk_eq);
+      bool sel[kPer];
+      int n_sel = 0;
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        sel[q] = gt[q] || (eq[q] && eq_rank < need);
+        eq_rank += eq[q];
+        n_sel += sel[q];
+      }
+      int pos = block_excl_scan(n_sel, wsum, &chunk_sel);
       // slots past n would belong to the window block: never written from here
       const int room = max(0, min(chunk_sel, n - (out_before + running)));
-      if (sel && pos < room) {
-        idx_out[out_before + running + pos] = j0 + jj;
-        sel_pos[pos] = j0 + jj;
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        if (sel[q]) {
+          if (pos < room) {
+            idx_out[out_before + running + pos] = j0 + x0 + q;
+            sel_pos[pos] = j0 + x0 + q;
+          }
+          ++pos;
+        }
       }
       eq_before += chunk_eq;
       __syncthreads();
@@ -261,8 +342,7 @@ select_gather(const __grid_constant__ Plan p, int cache_floats) {
     }
   }
 
-  // 4. the window rows: slots n .. C-1 take positions P .. L-1
-  // (W <= kMaxRows < kSelectThreads, so one pass covers the window)
+  // 5. the window rows: slots n .. C-1 take positions P .. L-1
   if (rank == CS - 1) {
     for (int w = t; w < p.W; w += blockDim.x) {
       idx_out[n + w] = P + w;
@@ -273,20 +353,88 @@ select_gather(const __grid_constant__ Plan p, int cache_floats) {
   }
 }
 
+namespace {
+
+int g_max_cluster = 0;  // largest cluster size this GPU allows for the kernel (16 or 8)
+
+size_t smem_for(int CS, int maxP, int kp) {
+  const int slice = (maxP + CS - 1) / CS;
+  const int need = kPoolTile + 2 * (kp / 2) + slice;
+  return (size_t)(need <= kStageFloats ? need : kPoolTile + 2 * (kp / 2)) * sizeof(float);
+}
+
+// Clusters of CS CTAs (with `smem` dynamic bytes each) that fit on the GPU at once.
+int max_active_clusters(int CS, size_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = CS;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(CS, 1);
+  cfg.blockDim = dim3(kSelectThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, select_gather, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+}  // namespace
+
 int launch_select_gather(const Plan& p, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int max_slice = 0;
-  for (int s = 0; s < p.nseq; ++s)
-    if (p.seq[s].scored) max_slice = max(max_slice, (p.seq[s].P + kClusterCTAs - 1) / kClusterCTAs);
-  const int cache_floats = min(max_slice, 48 * 1024);
-  const size_t smem = (size_t)cache_floats * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(select_gather, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)(smem > 0 ? smem : 1));
+                                       kStageFloats * (int)sizeof(float));
   if (e != cudaSuccess) return e;
-  dim3 grid(kClusterCTAs, p.nseq * p.H_kv);
-  select_gather<<<grid, kSelectThreads, smem, st>>>(p, cache_floats);
+  static int sms = 0;
+  if (g_max_cluster == 0) {
+    g_max_cluster = 8;
+    if (cudaFuncSetAttribute(select_gather, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess &&
+        max_active_clusters(kMaxCluster, 64 * 1024) > 0)
+      g_max_cluster = kMaxCluster;
+    cudaGetLastError();
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 1;
+  }
+  // Cluster size: a power of two, large enough that all units together fill
+  // the GPU and each slice fits the shared-memory staging, then halved while
+  // the clusters would not all be resident at once (one wave).
+  const int units = p.nseq * p.H_kv;
+  int maxP = 0;
+  for (int s = 0; s < p.nseq; ++s)
+    if (p.seq[s].scored) maxP = max(maxP, p.seq[s].P);
+  const int room = kStageFloats - kPoolTile - 2 * (p.kp / 2);
+  int CS = 1;
+  while (CS < g_max_cluster && (units * CS < sms || (maxP + CS - 1) / CS > room)) CS *= 2;
+  while (CS > 1 && (maxP + CS / 2 - 1) / (CS / 2) <= room &&
+         max_active_clusters(CS, smem_for(CS, maxP, p.kp)) < units)
+    CS /= 2;
+  const size_t smem = smem_for(CS, maxP, p.kp);
+  const int cap_floats = (int)(smem / sizeof(float));
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = CS;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(CS, units);
+  cfg.blockDim = dim3(kSelectThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, select_gather, p, cap_floats);
+  if (e != cudaSuccess) return e;
   count_launches(1);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace snapkv
