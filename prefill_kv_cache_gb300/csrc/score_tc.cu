@@ -21,10 +21,10 @@
 //   warps 2-9 two consumer warpgroups; warpgroup w reads TMEM buffer w, so
 //     the two groups take alternate key tiles.
 // Work items come from a device-wide queue in the order
-//   P1(0) | P1(1) M(0) P2(0) | P1(2) M(1) P2(1) | ... | M(G-1) P2(G-1)
+//   P1(0) | P1(1) M(0) | P1(2) M(1) P2(0) | ... | M(G-1) P2(G-2) | P2(G-1)
 // where a group is ~1024 key tiles of whole KV heads, P1 / P2 are pass-1 /
 // pass-2 pieces of 8 tiles and M are merge items.  Pass 2 of a group
-// re-reads K that pass 1 streamed through L2 one group earlier.  A merge item
+// re-reads K that pass 1 streamed through L2 two groups earlier.  A merge item
 // waits for its group's pass-1 pieces and a pass-2 item for its group's
 // merges; both always sit later in the queue than what they wait for, so
 // the waits cannot form a cycle whatever the number of resident CTAs.
@@ -715,18 +715,22 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken) {
     }
     G.m_items = ((G.u1 - G.u0) * p.Wp + kMergeRows - 1) / kMergeRows;
   }
-  // queue order: P1(0) | P1(1) M(0) P2(0) | ... | M(G-1) P2(G-1)
+  // queue order: P1(0) | P1(1) M(0) | P1(2) M(1) P2(0) | ... | M(G-1) P2(G-2) | P2(G-1):
+  // merges follow the next group's pass 1, pass 2 trails by two groups, so
+  // pass-2 items rarely wait for their merge while K is still in L2
   int idx = 0;
-  for (int k = 0; k <= g; ++k) {
+  for (int k = 0; k <= g + 1; ++k) {
     if (k < g) {
       tp.grp[k].p1_start = idx;
       idx += tp.grp[k].p1_items;
     }
-    if (k >= 1) {
+    if (k >= 1 && k - 1 < g) {
       tp.grp[k - 1].m_start = idx;
       idx += tp.grp[k - 1].m_items;
-      tp.grp[k - 1].p2_start = idx;
-      idx += tp.grp[k - 1].p2_items;
+    }
+    if (k >= 2) {
+      tp.grp[k - 2].p2_start = idx;
+      idx += tp.grp[k - 2].p2_items;
     }
   }
   tp.total_items = idx;
