@@ -137,6 +137,40 @@ int snapkv_score(const snapkv_shape *shape, const void *q_win, const void *k,
                  size_t workspace_bytes, void *stream);
 
 /*
+ * snapkv_compress and snapkv_score with the window rows' log-sum-exp given
+ * by the caller.  The prefill attention that precedes SnapKV already
+ * normalises every window query row over its causally visible keys (the
+ * scoring rides along with prefill: jisaku.com glossary "SnapKV", FAQ Q3);
+ * a caller that keeps that row normaliser passes it here and the library
+ * skips the first of its two sweeps over K (the per-row max and sum of
+ * exponentials), computing only the column sums of
+ *   exp(q_i . k_j / sqrt(d) - lse_win[b, i, head]).
+ *
+ *   lse_win   device, fp32, [B, W, H_q] row-major, 4-byte aligned: natural-
+ *             log LSE of window query i of sequence b and query head `head`,
+ *             log(sum_{j <= L_b - W + i} exp(q . k_j / sqrt(d))) over the
+ *             keys that query sees (its own position included), with q and
+ *             k exactly the q_win and k passed here.  Rows of sequences with
+ *             L_b <= C are not read.
+ *
+ * Every other argument, the workspace size, the outputs and the status
+ * behaviour are those of snapkv_compress / snapkv_score.  The values are
+ * trusted, not checked: a wrong LSE gives wrong scores (an LSE far below
+ * the true one can overflow them to +inf).  lse_win == NULL is
+ * SNAPKV_ERR_INVALID_ARG.
+ */
+int snapkv_compress_with_lse(const snapkv_shape *shape, const void *q_win, const void *k,
+                             const void *v, const float *lse_win,
+                             const int32_t *seqlens_host, int32_t W, int32_t kernel_size,
+                             int32_t pool_type, int32_t C, void *out_k, void *out_v,
+                             int32_t *out_idx, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+int snapkv_score_with_lse(const snapkv_shape *shape, const void *q_win, const void *k,
+                          const float *lse_win, const int32_t *seqlens_host, int32_t W,
+                          int32_t C, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Where the last snapkv_compress on this workspace left its fp32 score
  * vectors.  For every sequence with L_b > C and every KV head, the P_b =
  * L_b - W raw scores (window sums, group mean) and pooled scores are packed

@@ -52,6 +52,7 @@ struct Plan {
   float* pooled;     // same packing
   float2* stats;     // [total_pieces * Wp] (running max, sum of exp) per piece and row
   float* lse;        // [nseq * H_kv * Wp] natural-log LSE per (sequence, head, row)
+  const float* lse_in;  // caller's window LSE [B, W, H_q] (natural log), or null
   int* status;       // device status word
   int* counters;     // work-queue head and per-group completion counters
   long long total_rows;  // rows of k / v in the whole call (T)

@@ -161,8 +161,13 @@ score_pass2_simt(const __grid_constant__ Plan p) {
     const int i = row / p.g, member = row % p.g;
     qs[e] = qb[((size_t)(S.b * p.W + i) * p.H_q + (size_t)h * p.g + member) * D + cc];
   }
-  const float* lse = p.lse + (size_t)(s * p.H_kv + h) * p.Wp;
-  for (int row = threadIdx.x; row < p.Wp; row += blockDim.x) lse_s[row] = lse[row];
+  if (p.lse_in) {  // the caller's LSE, row = i * g + member
+    for (int row = threadIdx.x; row < p.Wp; row += blockDim.x)
+      lse_s[row] = p.lse_in[(size_t)(S.b * p.W + row / p.g) * p.H_q + (size_t)h * p.g + row % p.g];
+  } else {
+    const float* lse = p.lse + (size_t)(s * p.H_kv + h) * p.Wp;
+    for (int row = threadIdx.x; row < p.Wp; row += blockDim.x) lse_s[row] = lse[row];
+  }
   __syncthreads();
 
   const T* kbase = static_cast<const T*>(p.k);
@@ -186,13 +191,17 @@ score_pass2_simt(const __grid_constant__ Plan p) {
 
 template <typename T, int D>
 static int launch_simt_typed(const Plan& p, cudaStream_t st) {
-  dim3 g1(p.total_pieces, (p.Wp + kSimtThreads - 1) / kSimtThreads);
-  score_pass1_simt<T, D><<<g1, kSimtThreads, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  lse_merge<<<p.nseq * p.H_kv, kSimtThreads, 0, st>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
+  if (!p.lse_in) {  // pass 1 and the merge make the LSE; a caller's LSE replaces both
+    dim3 g1(p.total_pieces, (p.Wp + kSimtThreads - 1) / kSimtThreads);
+    score_pass1_simt<T, D><<<g1, kSimtThreads, 0, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    lse_merge<<<p.nseq * p.H_kv, kSimtThreads, 0, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launches(2);
+  }
   const size_t smem = (size_t)p.Wp * D * sizeof(T) + (size_t)p.Wp * sizeof(float);
   if (smem > 48 * 1024) {
     e = cudaFuncSetAttribute(score_pass2_simt<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -200,7 +209,7 @@ static int launch_simt_typed(const Plan& p, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   score_pass2_simt<T, D><<<p.total_pieces, kSimtThreads, smem, st>>>(p);
-  count_launches(3);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -56,6 +56,7 @@ constexpr int kMergeRows = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSmemLimit = 232448;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
+constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int { kP1 = 0, kMerge = 1, kP2 = 2, kDone = 3 };
 
@@ -528,9 +529,15 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       const SeqInfo& S = p.seq[s_idx];
       bool ok = true;
       if (e.type == kP2) {
-        if (ct == 0) wait_counter(&tp.counters[1 + tp.ngroups + e.g], G.m_items, ctl);
-        if (!csync() || *abort_flag) break;
-        for (int r = ct; r < wp; r += kConsumerThreads) aux[r] = __ldcg(p.lse + (size_t)e.u * wp + r);
+        if (p.lse_in) {  // the caller's natural-log LSE, row = i * g + member
+          for (int r = ct; r < wp; r += kConsumerThreads)
+            aux[r] = __ldg(p.lse_in + (size_t)(S.b * p.W + r / p.g) * p.H_q + (size_t)h * p.g +
+                           r % p.g) * kLog2e;
+        } else {
+          if (ct == 0) wait_counter(&tp.counters[1 + tp.ngroups + e.g], G.m_items, ctl);
+          if (!csync() || *abort_flag) break;
+          for (int r = ct; r < wp; r += kConsumerThreads) aux[r] = __ldcg(p.lse + (size_t)e.u * wp + r);
+        }
         if (!csync()) break;
       }
       // pass-1 running statistics of this thread's rows (R row blocks)
@@ -719,7 +726,16 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken) {
   // merges follow the next group's pass 1, pass 2 trails by two groups, so
   // pass-2 items rarely wait for their merge while K is still in L2
   int idx = 0;
-  for (int k = 0; k <= g + 1; ++k) {
+  if (p.lse_in) {  // the caller's LSE: pass 2 only
+    for (int k = 0; k < g; ++k) {
+      Group& G = tp.grp[k];
+      G.p1_items = G.m_items = 0;
+      G.p1_start = G.m_start = 1 << 30;
+      G.p2_start = idx;
+      idx += G.p2_items;
+    }
+  }
+  for (int k = 0; k <= g + 1 && !p.lse_in; ++k) {
     if (k < g) {
       tp.grp[k].p1_start = idx;
       idx += tp.grp[k].p1_items;

@@ -135,7 +135,7 @@ namespace {
 int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const void* v,
             const int32_t* seqlens_host, int32_t W, int32_t kernel_size, int32_t pool_type,
             int32_t C, void* out_k, void* out_v, int32_t* out_idx, void* workspace,
-            size_t workspace_bytes, void* stream, bool score_only) {
+            size_t workspace_bytes, void* stream, bool score_only, const float* lse_in) {
   int rc = check_problem(shape, seqlens_host, W, C);
   if (rc == SNAPKV_ERR_INVALID_ARG) return rc;
   if (!q_win || !k || !workspace) return SNAPKV_ERR_INVALID_ARG;
@@ -184,6 +184,7 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
   p.pooled = reinterpret_cast<float*>(ws + lay.pooled);
   p.stats = reinterpret_cast<float2*>(ws + lay.stats);
   p.lse = reinterpret_cast<float*>(ws + lay.lse);
+  p.lse_in = lse_in;
   p.status = reinterpret_cast<int*>(ws + lay.status);
   p.counters = reinterpret_cast<int*>(ws + lay.counters);
   p.batch = shape->batch;
@@ -227,14 +228,32 @@ int snapkv_compress(const snapkv_shape* shape, const void* q_win, const void* k,
                     int32_t pool_type, int32_t C, void* out_k, void* out_v, int32_t* out_idx,
                     void* workspace, size_t workspace_bytes, void* stream) {
   return enqueue(shape, q_win, k, v, seqlens_host, W, kernel_size, pool_type, C, out_k, out_v,
-                 out_idx, workspace, workspace_bytes, stream, false);
+                 out_idx, workspace, workspace_bytes, stream, false, nullptr);
 }
 
 int snapkv_score(const snapkv_shape* shape, const void* q_win, const void* k,
                  const int32_t* seqlens_host, int32_t W, int32_t C, void* workspace,
                  size_t workspace_bytes, void* stream) {
   return enqueue(shape, q_win, k, nullptr, seqlens_host, W, 1, SNAPKV_POOL_AVG, C, nullptr,
-                 nullptr, nullptr, workspace, workspace_bytes, stream, true);
+                 nullptr, nullptr, workspace, workspace_bytes, stream, true, nullptr);
+}
+
+int snapkv_compress_with_lse(const snapkv_shape* shape, const void* q_win, const void* k,
+                             const void* v, const float* lse_win, const int32_t* seqlens_host,
+                             int32_t W, int32_t kernel_size, int32_t pool_type, int32_t C,
+                             void* out_k, void* out_v, int32_t* out_idx, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!lse_win || !aligned(lse_win, 4)) return SNAPKV_ERR_INVALID_ARG;
+  return enqueue(shape, q_win, k, v, seqlens_host, W, kernel_size, pool_type, C, out_k, out_v,
+                 out_idx, workspace, workspace_bytes, stream, false, lse_win);
+}
+
+int snapkv_score_with_lse(const snapkv_shape* shape, const void* q_win, const void* k,
+                          const float* lse_win, const int32_t* seqlens_host, int32_t W, int32_t C,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (!lse_win || !aligned(lse_win, 4)) return SNAPKV_ERR_INVALID_ARG;
+  return enqueue(shape, q_win, k, nullptr, seqlens_host, W, 1, SNAPKV_POOL_AVG, C, nullptr,
+                 nullptr, nullptr, workspace, workspace_bytes, stream, true, lse_win);
 }
 
 uint64_t snapkv_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }

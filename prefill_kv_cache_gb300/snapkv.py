@@ -27,6 +27,8 @@ EXPORTED = (
     "snapkv_workspace_size",
     "snapkv_compress",
     "snapkv_score",
+    "snapkv_compress_with_lse",
+    "snapkv_score_with_lse",
     "snapkv_score_offsets",
     "snapkv_get_status",
     "snapkv_host_staging_size",
@@ -69,6 +71,11 @@ def load() -> ctypes.CDLL:
     lib.snapkv_compress.restype = ctypes.c_int
     lib.snapkv_score.argtypes = [shp, vp, vp, vp, i32, i32, vp, sz, vp]
     lib.snapkv_score.restype = ctypes.c_int
+    lib.snapkv_compress_with_lse.argtypes = [shp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp,
+                                             vp, vp, sz, vp]
+    lib.snapkv_compress_with_lse.restype = ctypes.c_int
+    lib.snapkv_score_with_lse.argtypes = [shp, vp, vp, vp, vp, i32, i32, vp, sz, vp]
+    lib.snapkv_score_with_lse.restype = ctypes.c_int
     lib.snapkv_kernel_launches.argtypes = []
     lib.snapkv_kernel_launches.restype = ctypes.c_uint64
     lib.snapkv_score_offsets.argtypes = [shp, vp, i32, i32, ctypes.POINTER(sz),
@@ -159,12 +166,14 @@ def compress(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seqlens,
              window_size: int, kernel_size: int, pooling, max_capacity_prompt: int,
              out_k: torch.Tensor | None = None, out_v: torch.Tensor | None = None,
              out_idx: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-             stream=None):
+             stream=None, lse_win: torch.Tensor | None = None):
     """Compress one layer (see include/snapkv.h, snapkv_compress).
 
     q_win [B, W, H_q, d], k / v [T, H_kv, d] (packed, bf16 or fp32, CUDA);
     seqlens: B host integers.  Returns (out_k, out_v, out_idx, workspace);
-    outputs that are not given are allocated here with torch.
+    outputs that are not given are allocated here with torch.  With lse_win
+    (fp32 [B, W, H_q], the window rows' natural-log LSE) the call goes to
+    snapkv_compress_with_lse.
     """
     B, W, H_q, d = q_win.shape
     H_kv = k.shape[1]
@@ -188,27 +197,71 @@ def compress(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seqlens,
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
     arr, _ = _seqlens_array(seqlens)
-    rc = load().snapkv_compress(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(), v.data_ptr(),
-                                arr, W, int(kernel_size), pool_code(pooling), C,
-                                out_k.data_ptr(), out_v.data_ptr(), out_idx.data_ptr(),
-                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                _stream_handle(stream))
+    if lse_win is not None:
+        _check_lse(lse_win, B, W, H_q)
+    ws_args = (workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+               _stream_handle(stream))
+    if lse_win is None:
+        rc = load().snapkv_compress(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(),
+                                    v.data_ptr(), arr, W, int(kernel_size), pool_code(pooling), C,
+                                    out_k.data_ptr(), out_v.data_ptr(), out_idx.data_ptr(),
+                                    *ws_args)
+        name = "snapkv_compress"
+    else:
+        rc = load().snapkv_compress_with_lse(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(),
+                                             v.data_ptr(), lse_win.data_ptr(), arr, W,
+                                             int(kernel_size), pool_code(pooling), C,
+                                             out_k.data_ptr(), out_v.data_ptr(),
+                                             out_idx.data_ptr(), *ws_args)
+        name = "snapkv_compress_with_lse"
     if rc:
-        raise SnapKVError(rc, "snapkv_compress")
+        raise SnapKVError(rc, name)
     return out_k, out_v, out_idx, workspace
 
 
+def _check_lse(lse_win: torch.Tensor, B: int, W: int, H_q: int) -> None:
+    if lse_win.dtype != torch.float32 or tuple(lse_win.shape) != (B, W, H_q) or \
+            not lse_win.is_contiguous():
+        raise ValueError(f"lse_win must be a contiguous float32 tensor of shape {(B, W, H_q)}")
+
+
+def compress_with_lse(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                      lse_win: torch.Tensor, seqlens, window_size: int, kernel_size: int, pooling,
+                      max_capacity_prompt: int, **kw):
+    """snapkv_compress_with_lse (include/snapkv.h): the caller gives the window
+    rows' log-sum-exp, so only the column-sum sweep over K runs."""
+    return compress(q_win, k, v, seqlens, window_size, kernel_size, pooling, max_capacity_prompt,
+                    lse_win=lse_win, **kw)
+
+
 def score(q_win: torch.Tensor, k: torch.Tensor, seqlens, window_size: int,
-          max_capacity_prompt: int, workspace: torch.Tensor, stream=None) -> None:
-    """Scoring step only (include/snapkv.h, snapkv_score); raw scores stay in workspace."""
+          max_capacity_prompt: int, workspace: torch.Tensor, stream=None,
+          lse_win: torch.Tensor | None = None) -> None:
+    """Scoring step only (include/snapkv.h, snapkv_score, or snapkv_score_with_lse
+    when lse_win is given); raw scores stay in workspace."""
     B, W, H_q, d = q_win.shape
     shape = make_shape(B, H_q, k.shape[1], d, q_win.dtype)
     arr, _ = _seqlens_array(seqlens)
-    rc = load().snapkv_score(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(), arr, W,
-                             int(max_capacity_prompt), workspace.data_ptr(),
-                             workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if lse_win is not None:
+        _check_lse(lse_win, B, W, H_q)
+    tail = (W, int(max_capacity_prompt), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if lse_win is None:
+        rc = load().snapkv_score(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(), arr, *tail)
+        name = "snapkv_score"
+    else:
+        rc = load().snapkv_score_with_lse(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(),
+                                          lse_win.data_ptr(), arr, *tail)
+        name = "snapkv_score_with_lse"
     if rc:
-        raise SnapKVError(rc, "snapkv_score")
+        raise SnapKVError(rc, name)
+
+
+def score_with_lse(q_win: torch.Tensor, k: torch.Tensor, lse_win: torch.Tensor, seqlens,
+                   window_size: int, max_capacity_prompt: int, workspace: torch.Tensor,
+                   stream=None) -> None:
+    """snapkv_score_with_lse (include/snapkv.h)."""
+    score(q_win, k, seqlens, window_size, max_capacity_prompt, workspace, stream, lse_win=lse_win)
 
 
 def kernel_launches() -> int:

@@ -16,6 +16,7 @@ import numpy as np
 import torch
 
 import oracle
+import synth
 from prefill_kv_cache_gb300 import snapkv as S
 
 RTOL = 1e-5
@@ -29,12 +30,44 @@ def to_device(a: np.ndarray, dev="cuda") -> torch.Tensor:
     return t.to(dev)
 
 
-def run_gpu(lay, k_pool, pool, C, dev="cuda"):
-    """One snapkv_compress on the layer; returns numpy outputs and scores."""
+def window_lse(lay, C, fill=np.nan):
+    """Natural-log LSE of every window query row over its visible keys.
+
+    fp64 on the CPU from the layer's (bf16-exact) inputs, returned as fp32
+    [B, W, H_q], the input of snapkv_compress_with_lse: row (b, i, head) is
+    log sum_{j <= L_b - W + i} exp(q . k_j / sqrt(d)) with k from the head's
+    KV group.  Sequences with L_b <= C are filled with `fill` (the library
+    must not read them).
+    """
+    B, W, H_q, d = lay.q_win.shape
+    g = H_q // lay.H_kv
+    out = np.full((B, W, H_q), fill, dtype=np.float32)
+    q_all = lay.q_win if lay.q_win.dtype != np.uint16 else synth.bf16_to_f32(lay.q_win)
+    k_all = lay.k if lay.k.dtype != np.uint16 else synth.bf16_to_f32(lay.k)
+    for b, L in enumerate(lay.seqlens):
+        L = int(L)
+        if L <= C:
+            continue
+        P = L - W
+        kb = torch.from_numpy(np.ascontiguousarray(k_all[lay.offsets[b]:lay.offsets[b] + L]))
+        kb = kb.to(torch.float64)
+        mask = torch.arange(L)[None, :] > (P + torch.arange(W))[:, None]  # [W, L]
+        for h in range(lay.H_kv):
+            q = torch.from_numpy(np.ascontiguousarray(q_all[b, :, h * g:(h + 1) * g]))
+            s = torch.einsum("imd,jd->mij", q.to(torch.float64), kb[:, h]) / np.sqrt(d)
+            s.masked_fill_(mask[None], -np.inf)
+            out[b, :, h * g:(h + 1) * g] = torch.logsumexp(s, dim=2).T.numpy()
+    return out
+
+
+def run_gpu(lay, k_pool, pool, C, dev="cuda", lse=None):
+    """One snapkv_compress (snapkv_compress_with_lse when `lse` is given) on
+    the layer; returns numpy outputs and scores."""
     q = to_device(lay.q_win, dev)
     k = to_device(lay.k, dev)
     v = to_device(lay.v, dev)
-    ok, ov, oi, ws = S.compress(q, k, v, lay.seqlens, lay.W, k_pool, pool, C)
+    lse_t = None if lse is None else to_device(lse, dev)
+    ok, ov, oi, ws = S.compress(q, k, v, lay.seqlens, lay.W, k_pool, pool, C, lse_win=lse_t)
     st = S.get_status(ws)
     assert st == S.OK, S.status_string(st)
     shape = S.make_shape(lay.B, lay.H_q, lay.H_kv, lay.d, q.dtype)

@@ -53,6 +53,39 @@ def test_invalid_arguments(kw):
     assert compress_rc(shape(), [4096], **kw) == S.ERR_INVALID_ARG
 
 
+def lse_rc(sh, seqlens, lse=FAKE, score_only=False, W=32, C=1024, ws_bytes=1 << 30, q=FAKE):
+    arr = (ctypes.c_int32 * len(seqlens))(*seqlens)
+    lib = S.load()
+    if score_only:
+        return lib.snapkv_score_with_lse(ctypes.byref(sh), q, FAKE, lse, arr, W, C, FAKE,
+                                         ws_bytes, None)
+    return lib.snapkv_compress_with_lse(ctypes.byref(sh), q, FAKE, FAKE, lse, arr, W, 5, 0, C,
+                                        FAKE, FAKE, FAKE, FAKE, ws_bytes, None)
+
+
+@pytest.mark.parametrize("score_only", [False, True])
+def test_lse_entry_points_check_arguments(score_only):
+    sh = shape()
+    assert lse_rc(sh, [4096], lse=None, score_only=score_only) == S.ERR_INVALID_ARG
+    assert lse_rc(sh, [4096], lse=FAKE + 2, score_only=score_only) == S.ERR_INVALID_ARG
+    assert lse_rc(sh, [4096], q=None, score_only=score_only) == S.ERR_INVALID_ARG
+    assert lse_rc(sh, [4096], W=0, score_only=score_only) == S.ERR_INVALID_ARG
+    assert lse_rc(shape(d=96), [4096], score_only=score_only) == S.ERR_UNSUPPORTED
+    need = S.workspace_size(sh, [20000], 32, 1024)
+    assert lse_rc(sh, [20000], ws_bytes=need - 1, score_only=score_only) == S.ERR_WORKSPACE
+
+
+def test_lse_binding_checks_tensor_shape():
+    import torch
+    q = torch.zeros(2, 4, 8, 64)
+    k = torch.zeros(100, 2, 64)
+    ws = torch.zeros(16, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        S.score_with_lse(q, k, torch.zeros(2, 4, 7), [50, 50], 4, 32, ws)
+    with pytest.raises(ValueError):
+        S.score_with_lse(q, k, torch.zeros(2, 4, 8, dtype=torch.float64), [50, 50], 4, 32, ws)
+
+
 def test_invalid_shapes():
     assert compress_rc(None, [4096]) == S.ERR_INVALID_ARG
     assert compress_rc(shape(), None) == S.ERR_INVALID_ARG

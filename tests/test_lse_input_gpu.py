@@ -1,0 +1,98 @@
+"""GPU parity of the LSE-input entry points (snapkv_compress_with_lse,
+snapkv_score_with_lse) against the CPU oracle.
+
+The caller's window LSE comes from tests/parity.window_lse (fp64 on the CPU,
+rounded to fp32 as a prefill kernel would return it).  With it the library
+runs only the column-sum sweep over K; the scores, the selection and the
+gathered rows must meet the same agreement rule as snapkv_compress
+(tests/parity.py).  Sequences kept whole get NaN LSE rows, which must never
+be read.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from prefill_kv_cache_gb300 import snapkv as S
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # seqlens,              H_q, H_kv, d,  W,  C,   k, pool,  dtype   (path)
+    ([1024],                  4,   4, 64, 16, 256,  5, "avg", "fp32"),  # SIMT
+    ([1025, 300, 2000],       8,   2, 128, 16, 256, 7, "max", "bf16"),  # SIMT (W*g = 64)
+    ([3000],                 32,   8, 128, 32, 1024, 13, "avg", "bf16"),  # tensor cores, 128 rows
+    ([5000, 1100, 40],       32,   8, 128, 32, 1024, 7, "max", "bf16"),
+    ([6000],                 32,   4, 128, 32, 2048, 9, "avg", "bf16"),  # 256 rows
+    ([8192, 700, 3100],      32,   8, 128, 64, 1024, 5, "max", "bf16"),
+    ([2049],                 16,   4, 64, 64, 512,  7, "avg", "bf16"),   # d = 64
+    ([33, 17, 1],             4,   2, 64, 16, 40,   5, "avg", "bf16"),   # all keep-all
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: f"L{c[0]}-g{c[1]//c[2]}-d{c[3]}-W{c[4]}-C{c[5]}-{c[7]}{c[6]}-{c[8]}")
+def test_small_shapes_with_lse(case):
+    seqlens, H_q, H_kv, d, W, C, kp, pool, dtype = case
+    lay = synth.make_inputs(177 + sum(seqlens), seqlens, H_q, H_kv, d, W, dtype, nspans=3)
+    lse = parity.window_lse(lay, C)
+    launches = S.kernel_launches()
+    gpu = parity.run_gpu(lay, kp, pool, C, lse=lse)
+    ora = parity.oracle_for(lay, kp, pool, C)
+    parity.check(lay, gpu, ora, C)
+    if any(L > C for L in seqlens):
+        # one score launch (tensor cores, or the pass-2 kernel alone), one selection
+        assert S.kernel_launches() - launches == 2
+
+
+@pytest.mark.parametrize("name,seqs", [("2", None), ("4", [0]), ("5a", [7, 8])])
+def test_workload_with_lse(name, seqs):
+    cfg = synth.CONFIGS[name]
+    lay = synth.make_layer(name)
+    lse = parity.window_lse(lay, cfg["C"])
+    gpu = parity.run_gpu(lay, cfg["k_pool"], cfg["pool"], cfg["C"], lse=lse)
+    ora = parity.oracle_for(lay, cfg["k_pool"], cfg["pool"], cfg["C"], seqs=seqs)
+    parity.check(lay, gpu, ora, cfg["C"], seqs=seqs)
+    for b in range(lay.B):
+        for h in range(lay.H_kv):
+            kept = set(gpu["idx"][b, h].tolist())
+            assert all(p in kept for p in lay.targets[b][h]), (b, h)
+
+
+def test_lse_mode_agrees_with_two_pass_mode():
+    """Same inputs through snapkv_compress and snapkv_compress_with_lse."""
+    cfg = synth.CONFIGS["3"]
+    lay = synth.make_layer("3")
+    lse = parity.window_lse(lay, cfg["C"])
+    a = parity.run_gpu(lay, cfg["k_pool"], cfg["pool"], cfg["C"])
+    b = parity.run_gpu(lay, cfg["k_pool"], cfg["pool"], cfg["C"], lse=lse)
+    np.testing.assert_allclose(b["raw"], a["raw"], rtol=2e-5, atol=1e-7)
+    np.testing.assert_allclose(b["pooled"], a["pooled"], rtol=2e-5, atol=1e-7)
+    # kept sets may differ only between scores within the tolerance of the
+    # (C-W)-th best pooled score
+    n = cfg["C"] - lay.W
+    pooled = parity.unpack_scores(a["pooled"], lay.seqlens, lay.H_kv, lay.W, cfg["C"])
+    for bi in range(lay.B):
+        for h in range(lay.H_kv):
+            po = pooled[bi][h]
+            tau = np.sort(po)[::-1][n - 1]
+            diff = set(a["idx"][bi, h, :n].tolist()) ^ set(b["idx"][bi, h, :n].tolist())
+            bad = [j for j in diff if abs(po[j] - tau) > 4e-5 * tau]
+            assert not bad, (bi, h, bad[:8])
+
+
+def test_score_with_lse_fills_raw_scores():
+    lay = synth.make_inputs(12, [4000, 900], 32, 8, 128, 32, "bf16", nspans=2)
+    C = 1024
+    lse = parity.window_lse(lay, C)
+    q, k = parity.to_device(lay.q_win), parity.to_device(lay.k)
+    shape = S.make_shape(lay.B, lay.H_q, lay.H_kv, lay.d, q.dtype)
+    ws = torch.zeros(S.workspace_size(shape, lay.seqlens, lay.W, C), dtype=torch.uint8,
+                     device="cuda")
+    S.score_with_lse(q, k, parity.to_device(lse), lay.seqlens, lay.W, C, ws)
+    assert S.get_status(ws) == S.OK
+    raw, _ = S.scores_from_workspace(ws, shape, lay.seqlens, lay.W, C)
+    ora = parity.oracle_for(lay, 1, "avg", C, seqs=[0])
+    got = parity.unpack_scores(raw.cpu().numpy(), lay.seqlens, lay.H_kv, lay.W, C)
+    np.testing.assert_allclose(got[0], np.stack(ora["raw"][0]), rtol=parity.RTOL,
+                               atol=parity.ATOL)
