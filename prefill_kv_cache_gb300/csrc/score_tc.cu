@@ -15,11 +15,14 @@
 //   pass 2 (S^T = K Q^T, keys on TMEM lanes): each thread sums
 //     exp2(logit * log2e / sqrt(d) - lse2) over all query rows of its key.
 //
-// Kernel shape: persistent, one CTA per SM, 10 warps:
+// Kernel shape: persistent, one CTA per SM, 12 warps:
 //   warp 0  TMA producer (K tiles of 128 keys, Q of the current KV head),
 //   warp 1  MMA issuer (single thread) and TMEM owner (512 columns),
-//   warps 2-9 two consumer warpgroups; warpgroup w reads TMEM buffer w, so
-//     the two groups take alternate key tiles.
+//   warps 2-3 idle (their warpgroup gives its registers to the consumers),
+//   warps 4-11 two consumer warpgroups; both read every tile's accumulator,
+//     group w its column half, and hand the TMEM buffer back as soon as the
+//     columns are in registers, so the MMA of the tile after next overlaps
+//     their exp2 work.  Pass-2 half sums meet in shared memory.
 // Work items come from a device-wide queue in the order
 //   P1(0) | P1(1) M(0) | P1(2) M(1) P2(0) | ... | M(G-1) P2(G-2) | P2(G-1)
 // where a group is ~1024 key tiles of whole KV heads, P1 / P2 are pass-1 /
@@ -44,7 +47,7 @@
 namespace snapkv {
 namespace tc {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // 3 warpgroups
 constexpr int kConsumerThreads = 256;
 constexpr int kTileKeys = 128;
 constexpr int kTilesPerPiece = 8;  // 1024 keys, the piece size of the stats layout
@@ -122,9 +125,11 @@ __device__ __forceinline__ void raise_timeout(const Ctl& c) {
 }
 
 // Bounded wait for the phase of parity `parity` of barrier b.  Returns false
-// when the CTA is aborting (flag already set, or this wait expired).
-__device__ __noinline__ bool wait_bar(uint64_t* b, uint32_t parity, const Ctl& c) {
-  if (mbar_test(b, parity)) return true;
+// when the CTA is aborting (flag already set, or this wait expired).  All of
+// it is inline: an out-of-line call on the MMA thread's per-tile path costs
+// hundreds of cycles of idle tensor pipe, and calls cannot sit in code whose
+// register count setmaxnreg changes.
+__device__ __forceinline__ bool wait_bar_slow(uint64_t* b, uint32_t parity, Ctl c) {
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test(b, parity)) return true;
@@ -137,9 +142,12 @@ __device__ __noinline__ bool wait_bar(uint64_t* b, uint32_t parity, const Ctl& c
     }
   }
 }
+__device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, const Ctl& c) {
+  return mbar_test(b, parity) || wait_bar_slow(b, parity, c);
+}
 
 // Bounded wait until *ctr >= target (device-scope acquire).
-__device__ __noinline__ bool wait_counter(const int* ctr, int target, const Ctl& c) {
+__device__ __forceinline__ bool wait_counter(const int* ctr, int target, const Ctl& c) {
   const uint64_t t0 = global_ns();
   for (;;) {
     int v;
@@ -209,6 +217,26 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Lowers this warp's register count (the whole warpgroup executes it).
+__device__ __forceinline__ void reg_dealloc() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
+}
+
+// Pass-2 sum over N query rows of one key: sum_r exp2(v[r] * c2 - lse2[r]).
+template <int N>
+__device__ __forceinline__ float row_sum(const float* v, const float* lse2, float c2) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < N; j += 4) {
+    const float4 m4 = *reinterpret_cast<const float4*>(lse2 + j);
+    a0 += ex2(fmaf(v[j], c2, -m4.x));
+    a1 += ex2(fmaf(v[j + 1], c2, -m4.y));
+    a2 += ex2(fmaf(v[j + 2], c2, -m4.z));
+    a3 += ex2(fmaf(v[j + 3], c2, -m4.w));
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
 // ------------------------------------------------------------ schedule ---
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -276,6 +304,9 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
   uint8_t* qbuf = smem;
   uint8_t* kbuf = smem + 2 * q_bytes;
   float* aux = reinterpret_cast<float*>(kbuf + (size_t)NS * k_bytes);  // 512 floats
+  // pass-2 partial sums of the second group, 2 x 128: the upper half of aux,
+  // which pass-2 items do not use (their LSE takes at most 256 floats)
+  float* part = aux + 256;
   uint64_t* bars = reinterpret_cast<uint64_t*>(aux + 512);
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
@@ -285,7 +316,9 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
   uint64_t* tempty = tfull + 2;
   uint64_t* sfull = tempty + 2;
   uint64_t* sempty = sfull + kRing;
-  uint64_t* cbar = sempty + kRing;  // consumer-group barrier (256 arrivals)
+  uint64_t* pfull = sempty + kRing;  // part[b] written (128 arrivals)
+  uint64_t* pempty = pfull + 2;      // part[b] read (128 arrivals)
+  uint64_t* cbar = pempty + 2;       // consumer-group barrier (256 arrivals)
   uint64_t* drain = cbar + 1;       // MMA drain at teardown
   Entry* ring = reinterpret_cast<Entry*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ring + kRing);
@@ -302,7 +335,9 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       mbar_init(&qfull[b], 1);
       mbar_init(&qempty[b], 1);
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], 8);  // the 8 consumer warps
+      mbar_init(&pfull[b], 128);
+      mbar_init(&pempty[b], 128);
     }
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&sfull[s], 1);
@@ -326,11 +361,17 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const float c2 = p.log2e_scale;  // log2(e) / sqrt(d)
+  // registers: the launch gives 168 per thread (384 x 168 = 64512); the
+  // producer / MMA warpgroup hands most of its share to the consumers, who
+  // hold a tile's 128 accumulator columns in registers:
+  // 128 x 40 + 256 x 232 = 64512.  Each role's branch sets its own count.
 
+  if (warp < 4) reg_dealloc();  // one instruction for the whole warpgroup
   if (warp == 0) {
     // ------------------------------------------------------ producer ---
     if (lane == 0) {
-      int ring_n = 0, item_n = 0, stage_n = 0;
+      int ring_n = 0, item_n = 0, st = 0;
+      uint32_t sph = 0;  // phase parity of stage st's current use
       int fills[kMaxStages] = {0, 0, 0, 0, 0, 0, 0, 0};
       int qfills[2] = {0, 0};
       for (;;) {
@@ -354,8 +395,7 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
         ++qfills[qb];
         bool ok = true;
         for (int t = 0; t < e.ntiles; ++t) {
-          const int st = stage_n % NS;
-          if (!wait_bar(&empty[st], ((stage_n / NS) & 1) ^ 1, ctl)) {
+          if (!wait_bar(&empty[st], sph ^ 1, ctl)) {
             ok = false;
             break;
           }
@@ -365,7 +405,10 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
             tma_load_3d(smem_addr(kbuf + st * k_bytes + hf * k_half_bytes), &tm_k, &full[st],
                         hf * 64, h, row);
           ++fills[st];
-          ++stage_n;
+          if (++st == NS) {
+            st = 0;
+            sph ^= 1;
+          }
         }
         ++item_n;
         if (!ok) break;
@@ -389,7 +432,8 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA ---
     if (lane == 0) {
-      int ring_n = 0, item_n = 0, stage_n = 0, tile_n = 0;
+      int ring_n = 0, item_n = 0, st = 0, tile_n = 0;
+      uint32_t sph = 0;
       const uint32_t id_p1 = idesc_bf16(128, 128);
       const uint32_t id_p2 = idesc_bf16(128, wp);
       const int R = wp / 128;
@@ -408,9 +452,8 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
         const uint32_t qa = smem_addr(qbuf + qb * q_bytes);
         bool ok = true;
         for (int t = 0; t < e.ntiles; ++t) {
-          const int st = stage_n % NS;
           const int ab = tile_n & 1;
-          if (!wait_bar(&full[st], (stage_n / NS) & 1, ctl) ||
+          if (!wait_bar(&full[st], sph, ctl) ||
               !wait_bar(&tempty[ab], ((tile_n >> 1) & 1) ^ 1, ctl)) {
             ok = false;
             break;
@@ -439,7 +482,10 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
           mma_commit(&empty[st]);
           mma_commit(&tfull[ab]);
           issued = true;
-          ++stage_n;
+          if (++st == NS) {
+            st = 0;
+            sph ^= 1;
+          }
           ++tile_n;
         }
         mma_commit(&qempty[qb]);
@@ -454,15 +500,16 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
         }
       }
     }
-  } else {
+  } else if (warp >= 4) {
     // ----------------------------------------------------- consumers ---
-    const int ct = threadIdx.x - 64;          // 0..255
-    const int wg = ct >> 7;                   // warpgroup: TMEM buffer it reads
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
+    const int ct = threadIdx.x - 128;         // 0..255
+    const int wg = ct >> 7;                   // warpgroup: column half it reads
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int lrow = quarter * 32 + lane;     // TMEM lane of this thread
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const int R = wp / 128;
-    int ring_n = 0, tile_n = 0;
+    int ring_n = 0, tile_n = 0, p2_n = 0;
     uint32_t cphase = 0;
     auto csync = [&]() -> bool {  // all 256 consumer threads
       mbar_arrive(cbar);
@@ -545,67 +592,90 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       float* raw_out = p.raw + S.score0 + (size_t)h * S.P;
       const float inv_g = 1.0f / (float)p.g;
       for (int t = 0; t < e.ntiles; ++t, ++tile_n) {
-        if ((tile_n & 1) != wg) continue;
-        if (!wait_bar(&tfull[wg], (tile_n >> 1) & 1, ctl)) {
+        const int ab = tile_n & 1;  // TMEM buffer of this tile; both groups read it
+        if (!wait_bar(&tfull[ab], (tile_n >> 1) & 1, ctl)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const int key0 = (e.tile0 + t) * kTileKeys;
-        const uint32_t tb = tmem + lane_addr + (uint32_t)wg * 256u;
+        const uint32_t tb = tmem + lane_addr + (uint32_t)ab * 256u;
+        // this group's column half: keys [64 wg, 64 wg + 64) of every row
+        // block (pass 1) or query rows [wp/2 wg, wp/2 (wg + 1)) (pass 2)
+        __syncwarp();  // tcgen05.ld is warp-collective
         if (e.type == kP1) {
-          for (int rb = 0; rb < R; ++rb) {
-            const int row = rb * 128 + lrow;
-            const int limit = min(S.P + row / p.g, S.L - 1);  // last visible key
-            __syncwarp();  // tcgen05.ld is warp-collective
-            tmem_load64(tb + (uint32_t)rb * 128u, s);
-            tmem_load64(tb + (uint32_t)rb * 128u + 64u, s + 64);
-            float tmax = -INFINITY;
-            if (key0 + kTileKeys - 1 <= limit) {
+          if (R == 2)
+            tmem_load64x2(tb + (uint32_t)wg * 64u, tb + 128u + (uint32_t)wg * 64u, s);
+          else
+            tmem_load64(tb + (uint32_t)wg * 64u, s);
+        } else {
+          if (wp == 256)
+            tmem_load64x2(tb + (uint32_t)wg * 128u, tb + (uint32_t)wg * 128u + 64u, s);
+          else
+            tmem_load64(tb + (uint32_t)wg * 64u, s);
+        }
+        // the accumulator is in registers: hand the buffer back to the MMA
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[ab]);
+        if (e.type == kP1) {
 #pragma unroll
-              for (int j = 0; j < kTileKeys; ++j) tmax = fmaxf(tmax, s[j]);
+          for (int rb = 0; rb < 2; ++rb) {
+            if (rb >= R) break;
+            float* v = s + rb * 64;
+            const int row = rb * 128 + lrow;
+            const int limit = min(S.P + row / p.g, S.L - 1) - (key0 + wg * 64);  // last visible
+            float tmax = -INFINITY;
+            if (limit >= 63) {
+#pragma unroll
+              for (int j = 0; j < 64; ++j) tmax = fmaxf(tmax, v[j]);
             } else {
 #pragma unroll
-              for (int j = 0; j < kTileKeys; ++j) {
-                if (key0 + j > limit) s[j] = -INFINITY;
-                tmax = fmaxf(tmax, s[j]);
+              for (int j = 0; j < 64; ++j) {
+                if (j > limit) v[j] = -INFINITY;
+                tmax = fmaxf(tmax, v[j]);
               }
             }
-            if (tmax != -INFINITY) {  // some key of this tile is visible to the row
+            if (tmax != -INFINITY) {  // some key of this half tile is visible to the row
               const float Mn = fmaxf(Mrow[rb], tmax * c2);
               float z = Zrow[rb] * ex2(Mrow[rb] - Mn);
               float z1 = 0.f, z2 = 0.f, z3 = 0.f;
 #pragma unroll
-              for (int j = 0; j < kTileKeys; j += 4) {
-                z += ex2(fmaf(s[j], c2, -Mn));
-                z1 += ex2(fmaf(s[j + 1], c2, -Mn));
-                z2 += ex2(fmaf(s[j + 2], c2, -Mn));
-                z3 += ex2(fmaf(s[j + 3], c2, -Mn));
+              for (int j = 0; j < 64; j += 4) {
+                z += ex2(fmaf(v[j], c2, -Mn));
+                z1 += ex2(fmaf(v[j + 1], c2, -Mn));
+                z2 += ex2(fmaf(v[j + 2], c2, -Mn));
+                z3 += ex2(fmaf(v[j + 3], c2, -Mn));
               }
               Zrow[rb] = (z + z1) + (z2 + z3);
               Mrow[rb] = Mn;
             }
           }
         } else {
-          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-          for (int c0 = 0; c0 < wp; c0 += 64) {
-            __syncwarp();
-            tmem_load64(tb + (uint32_t)c0, s);
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-              const float4 m4 = *reinterpret_cast<const float4*>(aux + c0 + j);
-              a0 += ex2(fmaf(s[j], c2, -m4.x));
-              a1 += ex2(fmaf(s[j + 1], c2, -m4.y));
-              a2 += ex2(fmaf(s[j + 2], c2, -m4.z));
-              a3 += ex2(fmaf(s[j + 3], c2, -m4.w));
+          const float acc = wp == 256 ? row_sum<128>(s, aux + wg * 128, c2)
+                                      : row_sum<64>(s, aux + wg * 64, c2);
+          // combine the two halves of this key's sum in shared memory
+          const int pb = p2_n & 1;
+          const uint32_t pph = (p2_n >> 1) & 1;
+          ++p2_n;
+          if (wg == 1) {
+            if (!wait_bar(&pempty[pb], pph ^ 1, ctl)) {
+              ok = false;
+              break;
             }
+            part[pb * 128 + lrow] = acc;
+            mbar_arrive(&pfull[pb]);
+          } else {
+            if (!wait_bar(&pfull[pb], pph, ctl)) {
+              ok = false;
+              break;
+            }
+            const float other = part[pb * 128 + lrow];
+            mbar_arrive(&pempty[pb]);
+            const int key = key0 + lrow;
+            if (key < S.P) raw_out[key] = (acc + other) * inv_g;
           }
-          const int key = key0 + lrow;
-          if (key < S.P) raw_out[key] = ((a0 + a1) + (a2 + a3)) * inv_g;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[wg]);
       }
       if (!ok) break;
       if (e.type == kP1) {
@@ -754,7 +824,8 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken) {
   const uint32_t halves = p.d / 64;
   const uint32_t q_bytes = (uint32_t)p.Wp * 128u * halves;
   const uint32_t k_bytes = (uint32_t)kTileKeys * 128u * halves;
-  const uint32_t misc = 512 * 4 + (2 * kMaxStages + 8 + 2 * kRing + 2) * 8 + kRing * sizeof(Entry) + 8;
+  const uint32_t misc =
+      512 * 4 + (2 * kMaxStages + 8 + 2 * kRing + 4 + 2) * 8 + kRing * sizeof(Entry) + 8;
   const long long room = (long long)kSmemLimit - 2 * (long long)q_bytes - misc;
   int stages = (int)(room / k_bytes);
   if (stages > 6) stages = 6;
