@@ -217,6 +217,12 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Device-scope release increment: the caller's writes (and those ordered
+// before it by a CTA barrier) are visible to whoever acquires the new count.
+__device__ __forceinline__ void red_release_add(int* ctr, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(v) : "memory");
+}
+
 // Lowers this warp's register count (the whole warpgroup executes it).
 __device__ __forceinline__ void reg_dealloc() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 40;" ::: "memory");
@@ -318,8 +324,9 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
   uint64_t* sempty = sfull + kRing;
   uint64_t* pfull = sempty + kRing;  // part[b] written (128 arrivals)
   uint64_t* pempty = pfull + 2;      // part[b] read (128 arrivals)
-  uint64_t* cbar = pempty + 2;       // consumer-group barrier (256 arrivals)
-  uint64_t* drain = cbar + 1;       // MMA drain at teardown
+  uint64_t* cbar = pempty + 2;       // both consumer groups (8 warp arrivals)
+  uint64_t* wbar = cbar + 1;         // per consumer group (4 warp arrivals each)
+  uint64_t* drain = wbar + 2;        // MMA drain at teardown
   Entry* ring = reinterpret_cast<Entry*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ring + kRing);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(abort_flag) + 1);
@@ -336,14 +343,15 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       mbar_init(&qempty[b], 1);
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 8);  // the 8 consumer warps
-      mbar_init(&pfull[b], 128);
-      mbar_init(&pempty[b], 128);
+      mbar_init(&pfull[b], 4);  // warp arrivals
+      mbar_init(&pempty[b], 4);
+      mbar_init(&wbar[b], 4);
     }
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&sfull[s], 1);
       mbar_init(&sempty[s], 9);  // MMA thread + 8 consumer warps
     }
-    mbar_init(cbar, kConsumerThreads);
+    mbar_init(cbar, kConsumerThreads / 32);
     mbar_init(drain, 1);
     *abort_flag = (smem_addr(smem) & 1023u) != 0 ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -510,11 +518,21 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const int R = wp / 128;
     int ring_n = 0, tile_n = 0, p2_n = 0;
-    uint32_t cphase = 0;
-    auto csync = [&]() -> bool {  // all 256 consumer threads
-      mbar_arrive(cbar);
+    uint32_t cphase = 0, wphase = 0;
+    // barriers over both consumer groups / this thread's group; a warp
+    // arrives once its lanes' prior writes are ordered by __syncwarp
+    auto csync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cbar);
       const bool r = wait_bar(cbar, cphase, ctl);
       cphase ^= 1;
+      return r;
+    };
+    auto wgsync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wbar[wg]);
+      const bool r = wait_bar(&wbar[wg], wphase, ctl);
+      wphase ^= 1;
       return r;
     };
     float s[kTileKeys];
@@ -564,9 +582,8 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
           M = Mn;
         }
         if (sub == 0 && u >= 0) p.lse[(size_t)u * wp + r] = M + log2f(Z);
-        __threadfence();
         if (!csync()) break;
-        if (ct == 0) atomicAdd(&tp.counters[1 + tp.ngroups + e.g], 1);
+        if (ct == 0) red_release_add(&tp.counters[1 + tp.ngroups + e.g], 1);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sempty[slot]);
         continue;
@@ -575,17 +592,22 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       const int s_idx = e.u / p.H_kv, h = e.u % p.H_kv;
       const SeqInfo& S = p.seq[s_idx];
       bool ok = true;
+      // pass 2: this group reads the LSE of its rows [wp/2 wg, wp/2 (wg + 1));
+      // the load is issued here and lands in shared memory after the first
+      // tile's accumulator wait, which hides its latency
+      const int half = wp >> 1, li = ct & 127;
+      float lv = 0.f;
       if (e.type == kP2) {
-        if (p.lse_in) {  // the caller's natural-log LSE, row = i * g + member
-          for (int r = ct; r < wp; r += kConsumerThreads)
-            aux[r] = __ldg(p.lse_in + (size_t)(S.b * p.W + r / p.g) * p.H_q + (size_t)h * p.g +
-                           r % p.g) * kLog2e;
-        } else {
+        if (!p.lse_in) {
           if (ct == 0) wait_counter(&tp.counters[1 + tp.ngroups + e.g], G.m_items, ctl);
           if (!csync() || *abort_flag) break;
-          for (int r = ct; r < wp; r += kConsumerThreads) aux[r] = __ldcg(p.lse + (size_t)e.u * wp + r);
         }
-        if (!csync()) break;
+        if (li < half) {
+          const int r = wg * half + li;
+          lv = p.lse_in ? __ldg(p.lse_in + (size_t)(S.b * p.W + r / p.g) * p.H_q +
+                                (size_t)h * p.g + r % p.g) * kLog2e  // caller's, row = i g + member
+                        : __ldcg(p.lse + (size_t)e.u * wp + r);
+        }
       }
       // pass-1 running statistics of this thread's rows (R row blocks)
       float Mrow[2] = {-INFINITY, -INFINITY}, Zrow[2] = {0.f, 0.f};
@@ -598,6 +620,13 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
           break;
         }
         tc_fence_after();
+        if (e.type == kP2 && t == 0) {
+          if (li < half) aux[wg * half + li] = lv;
+          if (!wgsync()) {
+            ok = false;
+            break;
+          }
+        }
         const int key0 = (e.tile0 + t) * kTileKeys;
         const uint32_t tb = tmem + lane_addr + (uint32_t)ab * 256u;
         // this group's column half: keys [64 wg, 64 wg + 64) of every row
@@ -664,14 +693,16 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
               break;
             }
             part[pb * 128 + lrow] = acc;
-            mbar_arrive(&pfull[pb]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pfull[pb]);
           } else {
             if (!wait_bar(&pfull[pb], pph, ctl)) {
               ok = false;
               break;
             }
             const float other = part[pb * 128 + lrow];
-            mbar_arrive(&pempty[pb]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&pempty[pb]);
             const int key = key0 + lrow;
             if (key < S.P) raw_out[key] = (acc + other) * inv_g;
           }
@@ -681,22 +712,27 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       if (e.type == kP1) {
         // merge the two groups' statistics of each row, then publish
         float2* comb = reinterpret_cast<float2*>(aux);
-        if (wg == 1)
-          for (int rb = 0; rb < R; ++rb) comb[rb * 128 + lrow] = make_float2(Mrow[rb], Zrow[rb]);
+        if (wg == 1) {
+#pragma unroll
+          for (int rb = 0; rb < 2; ++rb)
+            if (rb < R) comb[rb * 128 + lrow] = make_float2(Mrow[rb], Zrow[rb]);
+        }
         if (!csync()) break;
         if (wg == 0) {
           const size_t piece = (size_t)S.piece0 + (size_t)h * S.chunks + e.piece;
-          for (int rb = 0; rb < R; ++rb) {
+#pragma unroll
+          for (int rb = 0; rb < 2; ++rb) {
+            if (rb >= R) break;
             const float2 o = comb[rb * 128 + lrow];
             float M = Mrow[rb], Z = Zrow[rb];
             const float Mn = fmaxf(M, o.x);
             if (Mn != -INFINITY) Z = Z * ex2(M - Mn) + o.y * ex2(o.x - Mn);
             p.stats[piece * wp + rb * 128 + lrow] = make_float2(Mn, Z);
           }
-          __threadfence();
+          // the group's writes are ordered before one release of the counter
+          if (!wgsync()) break;
+          if (ct == 0) red_release_add(&tp.counters[1 + e.g], 1);
         }
-        if (!csync()) break;
-        if (ct == 0) atomicAdd(&tp.counters[1 + e.g], 1);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[slot]);
@@ -825,7 +861,7 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken) {
   const uint32_t q_bytes = (uint32_t)p.Wp * 128u * halves;
   const uint32_t k_bytes = (uint32_t)kTileKeys * 128u * halves;
   const uint32_t misc =
-      512 * 4 + (2 * kMaxStages + 8 + 2 * kRing + 4 + 2) * 8 + kRing * sizeof(Entry) + 8;
+      512 * 4 + (2 * kMaxStages + 8 + 2 * kRing + 4 + 2 + 2) * 8 + kRing * sizeof(Entry) + 8;
   const long long room = (long long)kSmemLimit - 2 * (long long)q_bytes - misc;
   int stages = (int)(room / k_bytes);
   if (stages > 6) stages = 6;
