@@ -20,8 +20,9 @@
 //   3. keep every position with a value above T and the lowest-positioned
 //      `need` positions equal to T (ties go to the lower position), in
 //      ascending order, via per-CTA counts and block prefix scans -- no sort;
-//   4. copy the kept K and V rows, then the W window rows, into the
-//      compressed cache with 16-byte vector loads and stores
+//   4. write the kept positions, then the W window positions, to the index
+//      output; after a cluster barrier every CTA copies an equal share of
+//      the C output rows (K and V) by bulk copies staged in shared memory
 //      (glossary, algorithm flow steps 3-4).
 //
 // A sequence with L <= C keeps all its rows; its cluster only copies.
@@ -39,9 +40,74 @@ constexpr int kWarps = kSelectThreads / 32;
 constexpr int kPer = 4;                        // consecutive positions per thread per pass
 constexpr int kChunk = kSelectThreads * kPer;  // positions per compaction pass
 constexpr int kMaxCluster = 16;
-constexpr int kPoolTile = 4096;                // raw scores staged per pooling step
+constexpr int kPoolTile = 8192;                // raw scores staged per pooling step
+constexpr int kLd = 16;                        // independent global loads in flight per thread
 constexpr int kStageFloats = 44 * 1024;         // dynamic shared memory, in floats
 static_assert(kMaxRows < kChunk, "window rows are copied in one pass");
+
+// Floats of the raw-score staging area for pooling half-width r: the tile,
+// its halo, rounded to whole float4 plus one float4 run of slack that the
+// vectorised window reads may touch past the last output.
+__host__ __device__ constexpr int raw_span(int r) { return ((kPoolTile + 2 * r + 3) & ~3) + 16; }
+
+// Pools m outputs from the staged raw scores: output x covers
+// sraw[x .. x + KP - 1] (the tile starts r positions left of its first
+// output).  Each thread takes 4 consecutive outputs, reads their KP + 3
+// inputs as float4 and sums / maxes them left to right -- the same order,
+// hence the same fp32 result, for every output.
+template <int KP, bool AVG>
+__device__ __forceinline__ void pool_run(const float* sraw, float* spool, float* gout, int m) {
+  constexpr int NV = (KP + 3 + 3) / 4;  // float4 reads per 4 outputs
+  for (int x = 4 * (int)threadIdx.x; x < m; x += 4 * (int)blockDim.x) {
+    float w[4 * NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const float4 f = *reinterpret_cast<const float4*>(sraw + x + 4 * v);
+      w[4 * v] = f.x;
+      w[4 * v + 1] = f.y;
+      w[4 * v + 2] = f.z;
+      w[4 * v + 3] = f.w;
+    }
+    float o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float acc = AVG ? 0.f : -INFINITY;
+#pragma unroll
+      for (int q = 0; q < KP; ++q) acc = AVG ? acc + w[i + q] : fmaxf(acc, w[i + q]);
+      o[i] = AVG ? acc / (float)KP : acc;
+    }
+    if (x + 3 < m) {
+      *reinterpret_cast<float4*>(spool + x) = make_float4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) gout[x + i] = o[i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (x + i < m) {
+          spool[x + i] = o[i];
+          gout[x + i] = o[i];
+        }
+    }
+  }
+}
+
+template <bool AVG>
+__device__ bool pool_dispatch(int kp, const float* sraw, float* spool, float* gout, int m) {
+  switch (kp) {
+    case 1: pool_run<1, AVG>(sraw, spool, gout, m); return true;
+    case 3: pool_run<3, AVG>(sraw, spool, gout, m); return true;
+    case 5: pool_run<5, AVG>(sraw, spool, gout, m); return true;
+    case 7: pool_run<7, AVG>(sraw, spool, gout, m); return true;
+    case 9: pool_run<9, AVG>(sraw, spool, gout, m); return true;
+    case 11: pool_run<11, AVG>(sraw, spool, gout, m); return true;
+    case 13: pool_run<13, AVG>(sraw, spool, gout, m); return true;
+    case 15: pool_run<15, AVG>(sraw, spool, gout, m); return true;
+    case 17: pool_run<17, AVG>(sraw, spool, gout, m); return true;
+    case 19: pool_run<19, AVG>(sraw, spool, gout, m); return true;
+    case 21: pool_run<21, AVG>(sraw, spool, gout, m); return true;
+    default: return false;
+  }
+}
 
 __device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -100,6 +166,92 @@ __device__ __forceinline__ void copy_rows(const Plan& p, const SeqInfo& S, int h
   }
 }
 
+// ---- bulk (TMA) row copies through shared memory ----
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Bounded wait for phase `parity` of barrier b (2 s); false on expiry, with
+// the status word set.
+__device__ bool bar_wait(uint64_t* b, uint32_t parity, int* status) {
+  uint64_t t0 = 0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n"
+        " selp.b32 %0, 1, 0, q;\n}\n"
+        : "=r"(done)
+        : "r"(saddr(b)), "r"(parity)
+        : "memory");
+    if (done) return true;
+    uint64_t t1;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+    if (t1 - t0 > 2000000000ull) {
+      atomicExch(status, kDevTimeout);
+      return false;
+    }
+  }
+}
+
+// Copies the K and V rows of sequence positions pos[0..cnt) (KV head h) to
+// output slots slot0.. : batches of rows are fetched into `stage` by bulk
+// copies that complete on `bar`, then written out by bulk stores.  Every
+// thread of the block calls it.  False if a wait expired.
+__device__ bool bulk_copy_rows(const Plan& p, const SeqInfo& S, int h, const int* pos, int cnt,
+                               int slot0, int row_bytes, unsigned char* stage, int stage_bytes,
+                               uint64_t* bar, uint32_t& phase) {
+  const int per = stage_bytes / (2 * row_bytes);  // rows per batch (K and V)
+  const char* kin = static_cast<const char*>(p.k);
+  const char* vin = static_cast<const char*>(p.v);
+  char* kout = static_cast<char*>(p.out_k);
+  char* vout = static_cast<char*>(p.out_v);
+  // the stage held generic-proxy data before: order it before async writes
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncthreads();
+  bool ok = true;
+  for (int i0 = 0; i0 < cnt && ok; i0 += per) {
+    const int m = min(per, cnt - i0);
+    if (threadIdx.x == 0)
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(bar)),
+                   "r"(2 * m * row_bytes)
+                   : "memory");
+    __syncthreads();
+    for (int i = threadIdx.x; i < 2 * m; i += blockDim.x) {
+      const int row = i >> 1;
+      const char* src = ((i & 1) ? vin : kin) +
+                        ((size_t)(S.row0 + pos[i0 + row]) * p.H_kv + h) * row_bytes;
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+              "r"(saddr(stage + (size_t)i * row_bytes)),
+          "l"(src), "r"(row_bytes), "r"(saddr(bar))
+          : "memory");
+    }
+    ok = __syncthreads_and(bar_wait(bar, phase, p.status));
+    if (!ok) {  // give the copies in flight one more bounded wait before leaving
+      bar_wait(bar, phase, p.status);
+      break;
+    }
+    phase ^= 1;
+    {
+      for (int i = threadIdx.x; i < 2 * m; i += blockDim.x) {
+        const int row = i >> 1;
+        char* dst = ((i & 1) ? vout : kout) +
+                    (((size_t)S.b * p.C + slot0 + i0 + row) * p.H_kv + h) * row_bytes;
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                     "r"(saddr(stage + (size_t)i * row_bytes)), "r"(row_bytes)
+                     : "memory");
+      }
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // stage reusable
+    }
+    __syncthreads();
+  }
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  return ok;
+}
+
 __global__ void __launch_bounds__(kSelectThreads, 2)
 select_gather(const __grid_constant__ Plan p, int cap_floats) {
   extern __shared__ __align__(16) float dyn[];  // [raw staging tile + halo][pooled slice]
@@ -110,6 +262,7 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
   __shared__ int sel_pos[kChunk];
   __shared__ int sh_digit, sh_above;
   __shared__ int sh_cnt[2];
+  __shared__ __align__(8) uint64_t bulk_bar;
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
@@ -119,6 +272,13 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
   const int s = unit / p.H_kv, h = unit % p.H_kv;
   const SeqInfo& S = p.seq[s];
   const int vecs = p.d * (p.dtype == 0 ? 2 : 4) / 16;
+  const int row_bytes = vecs * 16;
+  uint32_t bulk_phase = 0;
+  if (t == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&bulk_bar)) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
   int32_t* idx_out = p.out_idx + ((size_t)S.b * p.H_kv + h) * p.C;
 
   if (!S.scored) {
@@ -151,38 +311,43 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
   const int cnt = j1 - j0;
   const float* raw = p.raw + S.score0 + (size_t)h * P;
   float* pooled = p.pooled + S.score0 + (size_t)h * P;
-  const bool in_smem = kPoolTile + 2 * r + cnt <= cap_floats;
+  const bool in_smem = raw_span(r) + cnt <= cap_floats;
   float* sraw = dyn;
-  float* spool = dyn + kPoolTile + 2 * r;
+  float* spool = dyn + raw_span(r);
 
   // 1. pooling of this CTA's slice (zero padding outside [0, P)), the raw
   //    scores staged in shared memory one tile (plus halo) at a time
   if (in_smem) {
     for (int x0 = 0; x0 < cnt; x0 += kPoolTile) {
       const int m = min(kPoolTile, cnt - x0);
-      for (int x1 = t; x1 < m + 2 * r; x1 += 4 * blockDim.x) {  // 4 loads in flight
-        float v4[4];
+      for (int x1 = t; x1 < m + 2 * r; x1 += kLd * blockDim.x) {  // kLd loads in flight
+        float vl[kLd];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kLd; ++u) {
           const int x = x1 + u * blockDim.x;
           const int jj = j0 + x0 - r + x;
-          v4[u] = (x < m + 2 * r && jj >= 0 && jj < P) ? __ldcg(raw + jj) : 0.f;
+          vl[u] = (x < m + 2 * r && jj >= 0 && jj < P) ? __ldcg(raw + jj) : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (x1 + u * blockDim.x < m + 2 * r) sraw[x1 + u * blockDim.x] = v4[u];
+        for (int u = 0; u < kLd; ++u)
+          if (x1 + u * blockDim.x < m + 2 * r) sraw[x1 + u * blockDim.x] = vl[u];
       }
       __syncthreads();
-      for (int x = t; x < m; x += blockDim.x) {
-        float acc = 0.f, mx = -INFINITY;
-        for (int q = 0; q <= 2 * r; ++q) {
-          const float v = sraw[x + q];
-          acc += v;
-          mx = fmaxf(mx, v);
+      const bool done = p.pool == 0
+                            ? pool_dispatch<true>(p.kp, sraw, spool + x0, pooled + j0 + x0, m)
+                            : pool_dispatch<false>(p.kp, sraw, spool + x0, pooled + j0 + x0, m);
+      if (!done) {  // other window sizes
+        for (int x = t; x < m; x += blockDim.x) {
+          float acc = 0.f, mx = -INFINITY;
+          for (int q = 0; q <= 2 * r; ++q) {
+            const float v = sraw[x + q];
+            acc += v;
+            mx = fmaxf(mx, v);
+          }
+          const float v = p.pool == 0 ? acc / (float)p.kp : mx;
+          spool[x0 + x] = v;
+          pooled[j0 + x0 + x] = v;
         }
-        const float v = p.pool == 0 ? acc / (float)p.kp : mx;
-        spool[x0 + x] = v;
-        pooled[j0 + x0 + x] = v;
       }
       __syncthreads();
     }
@@ -204,6 +369,7 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
     // 2. radix select of the n-th largest value (digits of 11, 11 and 10 bits)
     unsigned prefix = 0, mask = 0;
     int need = n;
+    int my_gt = 0, my_eq = 0;  // this CTA's values above / equal to the threshold
     for (int pass = 0; pass < 3; ++pass) {
       const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
       const int nb = pass == 2 ? 1024 : 2048;
@@ -261,26 +427,26 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
         }
       }
       __syncthreads();
+      // this CTA's own values in bins above the chosen digit are above T;
+      // after the last digit, its values in that bin equal T
+      const int D = sh_digit;
+      int la = 0;
+      for (int b = D + 1 + t; b < nb; b += blockDim.x) la += (int)hist[b];
+      int la_tot;
+      block_excl_scan(la, wsum, &la_tot);
+      my_gt += la_tot;
+      if (pass == 2) my_eq = (int)hist[D];
       need -= sh_above;
-      prefix |= (unsigned)sh_digit << shift;
+      prefix |= (unsigned)D << shift;
       mask |= (unsigned)(nb - 1) << shift;
       __syncthreads();
     }
     const unsigned T = prefix;
 
     // 3. per-CTA counts above / equal to T, exchanged across the cluster
-    int my_gt = 0, my_eq = 0;
-    for (int x = t; x < cnt; x += blockDim.x) {
-      const unsigned u = __float_as_uint(vals[x]);
-      my_gt += u > T;
-      my_eq += u == T;
-    }
-    int tot_gt, tot_eq;
-    block_excl_scan(my_gt, wsum, &tot_gt);
-    block_excl_scan(my_eq, wsum, &tot_eq);
     if (t == 0) {
-      sh_cnt[0] = tot_gt;
-      sh_cnt[1] = tot_eq;
+      sh_cnt[0] = my_gt;
+      sh_cnt[1] = my_eq;
     }
     cluster.sync();
     int eq_before = 0, out_before = 0, eq_acc = 0;
@@ -296,8 +462,8 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
     }
     cluster.sync();  // nobody leaves while others still read its shared memory
 
-    // 4. ascending compaction of the slice, kPer consecutive positions per
-    //    thread per pass, with the row copies
+    // 4. ascending compaction of the slice into the index output, kPer
+    //    consecutive positions per thread per pass
     int running = 0;
     for (int base = 0; base < cnt; base += kChunk) {
       const int x0 = base + t * kPer;
@@ -327,29 +493,38 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
 #pragma unroll
       for (int q = 0; q < kPer; ++q) {
         if (sel[q]) {
-          if (pos < room) {
-            idx_out[out_before + running + pos] = j0 + x0 + q;
-            sel_pos[pos] = j0 + x0 + q;
-          }
+          if (pos < room) idx_out[out_before + running + pos] = j0 + x0 + q;
           ++pos;
         }
       }
       eq_before += chunk_eq;
-      __syncthreads();
-      copy_rows(p, S, h, sel_pos, room, out_before + running, vecs);
       running += chunk_sel;
-      __syncthreads();
     }
   }
 
   // 5. the window rows: slots n .. C-1 take positions P .. L-1
-  if (rank == CS - 1) {
-    for (int w = t; w < p.W; w += blockDim.x) {
-      idx_out[n + w] = P + w;
-      sel_pos[w] = P + w;
-    }
+  if (rank == CS - 1)
+    for (int w = t; w < p.W; w += blockDim.x) idx_out[n + w] = P + w;
+
+  // 6. every CTA copies an equal share of the C output slots (kept rows
+  //    cluster together, so the slices' own kept rows would be unbalanced),
+  //    reading the positions back from the index output
+  cluster.sync();
+  const int share = (p.C + CS - 1) / CS;
+  const int s0 = min(p.C, rank * share), s1 = min(p.C, s0 + share);
+  const bool bulk = cap_floats * 4 >= 2 * row_bytes;
+  for (int c0 = s0; c0 < s1; c0 += kChunk) {
+    const int m = min(kChunk, s1 - c0);
+    __syncthreads();  // sel_pos free
+    for (int i = t; i < m; i += blockDim.x) sel_pos[i] = __ldcg(idx_out + c0 + i);
     __syncthreads();
-    copy_rows(p, S, h, sel_pos, p.W, n, vecs);
+    if (bulk) {
+      if (!bulk_copy_rows(p, S, h, sel_pos, m, c0, row_bytes, reinterpret_cast<unsigned char*>(dyn),
+                          cap_floats * 4, &bulk_bar, bulk_phase))
+        break;
+    } else {
+      copy_rows(p, S, h, sel_pos, m, c0, vecs);
+    }
   }
 }
 
@@ -359,8 +534,8 @@ int g_max_cluster = 0;  // largest cluster size this GPU allows for the kernel (
 
 size_t smem_for(int CS, int maxP, int kp) {
   const int slice = (maxP + CS - 1) / CS;
-  const int need = kPoolTile + 2 * (kp / 2) + slice;
-  return (size_t)(need <= kStageFloats ? need : kPoolTile + 2 * (kp / 2)) * sizeof(float);
+  const int need = raw_span(kp / 2) + slice;
+  return (size_t)(need <= kStageFloats ? need : raw_span(kp / 2)) * sizeof(float);
 }
 
 // Clusters of CS CTAs (with `smem` dynamic bytes each) that fit on the GPU at once.
@@ -411,7 +586,7 @@ int launch_select_gather(const Plan& p, void* stream) {
   int maxP = 0;
   for (int s = 0; s < p.nseq; ++s)
     if (p.seq[s].scored) maxP = max(maxP, p.seq[s].P);
-  const int room = kStageFloats - kPoolTile - 2 * (p.kp / 2);
+  const int room = kStageFloats - raw_span(p.kp / 2);
   int CS = 1;
   while (CS < g_max_cluster && (units * CS < sms || (maxP + CS - 1) / CS > room)) CS *= 2;
   while (CS > 1 && (maxP + CS / 2 - 1) / (CS / 2) <= room &&
