@@ -240,6 +240,58 @@ int snapkv_compress_noalloc(const snapkv_shape *shape, const void *q_win, const 
                             int32_t kernel_size, int32_t pool_type, int32_t C, void *out_k,
                             void *out_v, int32_t *out_idx, void *stream);
 
+/*
+ * ---- Decode step over a KV cache ----
+ *
+ * After compression the generation (decode) phase attends over the
+ * compressed cache instead of the full one (jisaku.com glossary "SnapKV",
+ * "SnapKVの仕組み", algorithm flow step 4), which relieves the memory-bandwidth
+ * bound of decoding (glossary FAQ Q2; hotpaper.ai summary of "SnapKV: LLM
+ * Knows What You are Looking for Before Generation", "주요 결과").
+ * snapkv_decode_attention computes one decode step of attention for one
+ * query token per sequence:
+ *
+ *   out[b, hq, :] = sum_j softmax_j(q[b, hq] . k[b, j, h] / sqrt(d)) v[b, j, h]
+ *
+ * with h = hq / g, over the lens[b] cached rows j of sequence b (no mask: the
+ * caller appends the new token's own key and value to the cache if it is to
+ * be attended).
+ */
+typedef enum {
+  SNAPKV_CACHE_PACKED = 0, /* k, v [sum_b lens[b], H_kv, d]: sequences back to back
+                              (the layout snapkv_compress takes: the full cache) */
+  SNAPKV_CACHE_SLOTS = 1   /* k, v [B, C, H_kv, d]: sequence b's rows are its slots
+                              0 .. lens[b]-1 (snapkv_compress's outputs, with
+                              lens[b] = min(L_b, C)) */
+} snapkv_cache_layout;
+
+/*
+ * Workspace bytes for snapkv_decode_attention (0 if the arguments are
+ * invalid or unsupported).  lens_host: host, B entries.
+ */
+size_t snapkv_decode_workspace_size(const snapkv_shape *shape, const int32_t *lens_host,
+                                    int32_t layout, int32_t C);
+
+/*
+ *   shape      B, H_q, H_kv (H_q / H_kv in {1, 2, 4, 8, 16}), d in {64, 128},
+ *              dtype of q, k and v (bf16 or fp32).
+ *   q          device, [B, H_q, d], 16-byte aligned.
+ *   k_cache    device, layout per `layout`, 16-byte aligned; v_cache likewise.
+ *   lens_host  host, B entries, each >= 1 (and <= C for SNAPKV_CACHE_SLOTS).
+ *   C          slots per sequence for SNAPKV_CACHE_SLOTS (ignored otherwise).
+ *   out        device, fp32 [B, H_q, d], 16-byte aligned.
+ *   workspace  device, 16-byte aligned, >= snapkv_decode_workspace_size bytes.
+ *   stream     cudaStream_t.
+ * Returns SNAPKV_OK, SNAPKV_ERR_INVALID_ARG (null or misaligned pointer, bad
+ * lens, layout or shape), SNAPKV_ERR_UNSUPPORTED (d or group size),
+ * SNAPKV_ERR_WORKSPACE or SNAPKV_ERR_CUDA; nothing is enqueued on argument
+ * errors.  Asynchronous; allocates nothing.
+ */
+int snapkv_decode_attention(const snapkv_shape *shape, const void *q, const void *k_cache,
+                            const void *v_cache, int32_t layout, const int32_t *lens_host,
+                            int32_t C, float *out, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
 /* Static text for a status code. */
 const char *snapkv_status_string(int status);
 

@@ -29,6 +29,8 @@ EXPORTED = (
     "snapkv_score",
     "snapkv_compress_with_lse",
     "snapkv_score_with_lse",
+    "snapkv_decode_workspace_size",
+    "snapkv_decode_attention",
     "snapkv_score_offsets",
     "snapkv_get_status",
     "snapkv_host_staging_size",
@@ -76,6 +78,10 @@ def load() -> ctypes.CDLL:
     lib.snapkv_compress_with_lse.restype = ctypes.c_int
     lib.snapkv_score_with_lse.argtypes = [shp, vp, vp, vp, vp, i32, i32, vp, sz, vp]
     lib.snapkv_score_with_lse.restype = ctypes.c_int
+    lib.snapkv_decode_workspace_size.argtypes = [shp, vp, i32, i32]
+    lib.snapkv_decode_workspace_size.restype = sz
+    lib.snapkv_decode_attention.argtypes = [shp, vp, vp, vp, i32, vp, i32, vp, vp, sz, vp]
+    lib.snapkv_decode_attention.restype = ctypes.c_int
     lib.snapkv_kernel_launches.argtypes = []
     lib.snapkv_kernel_launches.restype = ctypes.c_uint64
     lib.snapkv_score_offsets.argtypes = [shp, vp, i32, i32, ctypes.POINTER(sz),
@@ -331,3 +337,46 @@ def compress_noalloc(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seql
                                         _stream_handle(stream))
     if rc:
         raise SnapKVError(rc, "snapkv_compress_noalloc")
+
+
+# ---- decode step over a KV cache (include/snapkv.h, snapkv_decode_attention) ----
+
+CACHE_PACKED, CACHE_SLOTS = 0, 1
+
+
+def decode_workspace_size(shape: snapkv_shape, lens, layout: int, C: int = 0) -> int:
+    arr, _ = _seqlens_array(lens)
+    return int(load().snapkv_decode_workspace_size(ctypes.byref(shape), arr, int(layout), int(C)))
+
+
+def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, lens,
+                     layout: int, C: int = 0, out: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """One decode step of attention (include/snapkv.h, snapkv_decode_attention).
+
+    q [B, H_q, d]; k_cache / v_cache [sum(lens), H_kv, d] (CACHE_PACKED) or
+    [B, C, H_kv, d] (CACHE_SLOTS, rows 0..lens[b]-1 of each sequence); bf16 or
+    fp32, CUDA.  Returns fp32 [B, H_q, d].
+    """
+    B, H_q, d = q.shape
+    H_kv = k_cache.shape[-2]
+    shape = make_shape(B, H_q, H_kv, d, q.dtype)
+    arr, _ = _seqlens_array(lens)
+    if out is None:
+        out = torch.empty((B, H_q, d), dtype=torch.float32, device=q.device)
+    ws_bytes = decode_workspace_size(shape, lens, layout, C)
+    if ws_bytes == 0:
+        raise SnapKVError(ERR_INVALID_ARG, "snapkv_decode_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    rc = load().snapkv_decode_attention(ctypes.byref(shape), q.data_ptr(), k_cache.data_ptr(),
+                                        v_cache.data_ptr(), int(layout), arr, int(C),
+                                        out.data_ptr(), workspace.data_ptr(),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream_handle(stream))
+    if rc:
+        raise SnapKVError(rc, "snapkv_decode_attention")
+    return out

@@ -146,3 +146,36 @@ def test_binding_defaults_follow_page_example():
     assert (cfg.window_size, cfg.max_capacity_prompt, cfg.kernel_size, cfg.pooling) == (
         d["window_size"], d["max_capacity_prompt"], d["kernel_size"], d["pooling"])
     assert S.pool_code("avgpool") == S.POOL_AVG and S.pool_code("maxpool") == S.POOL_MAX
+
+
+def decode_rc(sh, lens, layout=0, C=0, q=FAKE, k=FAKE, v=FAKE, out=FAKE, ws=FAKE, ws_bytes=1 << 30):
+    arr = (ctypes.c_int32 * len(lens))(*lens)
+    return S.load().snapkv_decode_attention(ctypes.byref(sh), q, k, v, layout, arr, C, out, ws,
+                                            ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=None), dict(k=None), dict(v=None), dict(out=None), dict(ws=None), dict(q=FAKE + 8),
+    dict(out=FAKE + 4), dict(layout=2), dict(layout=-1),
+])
+def test_decode_invalid_arguments(kw):
+    assert decode_rc(shape(), [100], **kw) == S.ERR_INVALID_ARG
+
+
+def test_decode_invalid_and_unsupported_shapes():
+    assert decode_rc(shape(B=2), [100, 0]) == S.ERR_INVALID_ARG
+    assert decode_rc(shape(), [100], layout=S.CACHE_SLOTS, C=64) == S.ERR_INVALID_ARG  # lens > C
+    assert decode_rc(shape(), [100], layout=S.CACHE_SLOTS, C=0) == S.ERR_INVALID_ARG
+    assert decode_rc(shape(Hq=30), [100]) == S.ERR_INVALID_ARG
+    assert decode_rc(shape(d=96), [100]) == S.ERR_UNSUPPORTED
+    assert decode_rc(shape(Hq=24, Hkv=8), [100]) == S.ERR_UNSUPPORTED  # group of 3
+    assert decode_rc(shape(Hq=64, Hkv=2), [100]) == S.ERR_UNSUPPORTED  # group of 32
+
+
+def test_decode_workspace():
+    sh = shape(B=3)
+    assert S.decode_workspace_size(sh, [0, 5, 5], S.CACHE_PACKED) == 0
+    need = S.decode_workspace_size(sh, [1000, 5, 70000], S.CACHE_PACKED)
+    assert need > 0
+    assert S.decode_workspace_size(sh, [1000, 5, 80000], S.CACHE_PACKED) >= need
+    assert decode_rc(sh, [1000, 5, 70000], ws_bytes=need - 1) == S.ERR_WORKSPACE
