@@ -315,6 +315,8 @@ def main():
         except Exception:
             traffic = None
 
+    decode = decode_step(S, torch, data, outs, seqlens, cfg, dev, stream, peak)
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(S, torch, data, seqlens, cfg, shape, dev, stream, args, layers)
@@ -346,12 +348,71 @@ def main():
                                   "frac": compress_gbs / peak, "bytes_per_layer": compress_bytes},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "decode": decode,
             "gpu_launches": launches,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def decode_step(S, torch, data, outs, seqlens, cfg, dev, stream, peak, reps=5):
+    """One decode step (one query token per sequence) through every layer,
+    over the full prompt cache and over the compressed cache the timed
+    compression just wrote (snapkv_decode_attention; the decode phase of the
+    glossary's algorithm flow, step 4).  Each layer's cache is its own buffer,
+    so the 32-layer sweep streams from HBM."""
+    B = len(seqlens)
+    H_q, H_kv, d, C = cfg["H_q"], cfg["H_kv"], cfg["d"], cfg["C"]
+    dt = data[0][1].dtype
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(77)
+    qs = [torch.randn((B, H_q, d), generator=gen, device=dev).to(dt) for _ in data]
+    lens_c = [min(int(L), C) for L in seqlens]
+    shape = S.make_shape(B, H_q, H_kv, d, dt)
+    ws = torch.empty(max(S.decode_workspace_size(shape, seqlens, S.CACHE_PACKED),
+                         S.decode_workspace_size(shape, lens_c, S.CACHE_SLOTS, C)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((B, H_q, d), dtype=torch.float32, device=dev)
+
+    def sweep(compressed, st):
+        for q, (_, k, v), (ok, ov, _) in zip(qs, data, outs):
+            if compressed:
+                S.decode_attention(q, ok, ov, lens_c, S.CACHE_SLOTS, C, out=out, workspace=ws,
+                                   stream=st)
+            else:
+                S.decode_attention(q, k, v, seqlens, S.CACHE_PACKED, out=out, workspace=ws,
+                                   stream=st)
+
+    # the sweep is captured in a CUDA graph, so host launch cost is not timed
+    # (a decode step's per-layer kernels are short)
+    res = {}
+    cap = torch.cuda.Stream(device=dev)
+    for tag, comp, rows in (("full", False, sum(seqlens)), ("compressed", True, sum(lens_c))):
+        for _ in range(3):
+            sweep(comp, stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            sweep(comp, cap)
+        graph.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = 1e3 * a.elapsed_time(b) / reps / len(data)
+        nbytes = 2 * rows * H_kv * d * data[0][1].element_size()
+        res[f"us_per_layer_{tag}"] = us
+        res[f"gbs_{tag}"] = nbytes / us / 1e3
+        res[f"frac_{tag}"] = nbytes / us / 1e3 / peak
+    res["speedup"] = res["us_per_layer_full"] / res["us_per_layer_compressed"]
+    res["note"] = ("one query token per sequence, all layers back to back in one CUDA graph; "
+                   "K and V bytes read once per layer are the roofline bytes")
+    return res
 
 
 def run_e2e(S, torch, data, seqlens, cfg, shape, dev, stream, args, layers):

@@ -42,6 +42,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kGroup = 512;        // sequences per launch (kernel-parameter table)
 constexpr int kMinChunk = 128;     // keys per CTA, bounds
 constexpr int kMaxChunk = 2048;
+constexpr int kVUnroll = 8;        // V rows loaded ahead of their multiply-adds
 
 struct Seq {
   long long row0;  // first cache row of the sequence (a row = H_kv * d elements)
@@ -136,17 +137,20 @@ __global__ void __launch_bounds__(kThreads) decode_chunk(const __grid_constant__
   float* wml = qs + G * D;               // [kWarps][G][2]
   float* wacc = wml + kWarps * G * 2;    // [kWarps][G][D]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
+  // persistent: units (chunk, KV head), the heads of a chunk side by side
+  for (int unit_i = blockIdx.x; unit_i < p.total_chunks * p.H_kv; unit_i += gridDim.x) {
+  const int ch = unit_i / p.H_kv, h = unit_i % p.H_kv;
   // the sequence of this chunk
   int lo = 0, hi = p.nseq - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.seq[mid].chunk0 <= (int)blockIdx.x) lo = mid; else hi = mid - 1;
+    if (p.seq[mid].chunk0 <= ch) lo = mid; else hi = mid - 1;
   }
   const Seq& S = p.seq[lo];
   const int b = p.b0 + lo;
-  const int j0 = ((int)blockIdx.x - S.chunk0) * p.chunk;
+  const int j0 = (ch - S.chunk0) * p.chunk;
   const int j1 = min(S.n, j0 + p.chunk);
+  __syncthreads();  // the previous unit's shared-memory readers are done
 
   const T* qb = static_cast<const T*>(p.q) + ((size_t)b * p.H_q + (size_t)h * G) * D;
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
@@ -182,8 +186,8 @@ __global__ void __launch_bounds__(kThreads) decode_chunk(const __grid_constant__
     for (int x = 0; x < G; ++x) s[x] = 0.f;
     if (live) {
       const T* kr = kbase + (size_t)j * row_elems;
-#pragma unroll 4
-      for (int c = 0; c < D; c += 8) {
+#pragma unroll
+      for (int c = 0; c < D; c += 8) {  // all of the row's loads in flight at once
         float kf[8];
         load8<T>(kr + c, kf);
 #pragma unroll
@@ -214,14 +218,22 @@ __global__ void __launch_bounds__(kThreads) decode_chunk(const __grid_constant__
       m[x] = mn;
     }
     const int nk = min(32, wj1 - base);
-    for (int jj = 0; jj < nk; ++jj) {
-      float vf[DL];
-      load_cols<T, DL>(vbase + (size_t)(base + jj) * row_elems + lane * DL, vf);
+    for (int j8 = 0; j8 < nk; j8 += kVUnroll) {
+      float vf[kVUnroll][DL];  // kVUnroll rows' loads in flight
 #pragma unroll
-      for (int x = 0; x < G; ++x) {
-        const float w = __shfl_sync(0xffffffffu, pw[x], jj);
+      for (int u = 0; u < kVUnroll; ++u) {
+        const int jj = min(j8 + u, nk - 1);  // past the block end: a row already loaded, weight 0
+        load_cols<T, DL>(vbase + (size_t)(base + jj) * row_elems + lane * DL, vf[u]);
+      }
 #pragma unroll
-        for (int c = 0; c < DL; ++c) acc[x][c] = fmaf(w, vf[c], acc[x][c]);
+      for (int u = 0; u < kVUnroll; ++u) {
+#pragma unroll
+        for (int x = 0; x < G; ++x) {
+          float w = __shfl_sync(0xffffffffu, pw[x], (j8 + u) & 31);
+          if (j8 + u >= nk) w = 0.f;
+#pragma unroll
+          for (int c = 0; c < DL; ++c) acc[x][c] = fmaf(w, vf[u][c], acc[x][c]);
+        }
       }
     }
   }
@@ -236,7 +248,7 @@ __global__ void __launch_bounds__(kThreads) decode_chunk(const __grid_constant__
     for (int c = 0; c < DL; ++c) wacc[(warp * G + x) * D + lane * DL + c] = acc[x][c];
   }
   __syncthreads();
-  const size_t unit = (size_t)blockIdx.x * p.H_kv + h;
+  const size_t unit = (size_t)unit_i;
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
     const int x = i / D, c = i % D;
     float M = -INFINITY;
@@ -255,6 +267,7 @@ __global__ void __launch_bounds__(kThreads) decode_chunk(const __grid_constant__
     }
     p.part_o[unit * G * D + i] = O;
     if (c == 0) p.part_ml[unit * G + x] = make_float2(M, L);
+  }
   }
 }
 
@@ -279,15 +292,30 @@ __global__ void decode_combine(const __grid_constant__ Params p) {
   p.out[((size_t)(p.b0 + s) * p.H_q + hq) * p.d + c] = O / L;
 }
 
+int sm_count() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  return sms;
+}
+
 template <typename T, int D>
 cudaError_t launch_typed(const Params& p, cudaStream_t st) {
   const size_t smem = ((size_t)p.g * D + kWarps * p.g * 2 + (size_t)kWarps * p.g * D) * sizeof(float);
-  dim3 grid(p.total_chunks, p.H_kv);
+  const int units = p.total_chunks * p.H_kv;
   cudaError_t e = cudaSuccess;
   auto go = [&](auto kern) {
     if (smem > 48 * 1024)
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    int per_sm = 0;
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
     if (e == cudaSuccess) {
+      const int grid = std::max(1, std::min(units, sm_count() * std::max(per_sm, 1)));
       kern<<<grid, kThreads, smem, st>>>(p);
       e = cudaGetLastError();
     }
@@ -307,24 +335,13 @@ cudaError_t launch_typed(const Params& p, cudaStream_t st) {
   return e;
 }
 
-int sm_count() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
-  return sms;
-}
-
-// Keys per CTA: about two CTAs per SM over the whole launch, a power of two
-// in [kMinChunk, kMaxChunk].
+// Keys per unit: about eight units per SM over the launch (the persistent
+// CTAs then finish within a fraction of a unit of each other), a multiple of
+// 32 in [kMinChunk, kMaxChunk].
 int chunk_for(long long total_rows, int H_kv, int sms) {
-  const long long want = (total_rows * H_kv + 2LL * sms - 1) / (2LL * sms);
-  int c = kMinChunk;
-  while (c < kMaxChunk && c < want) c *= 2;
-  return c;
+  const long long want = (total_rows * H_kv + 8LL * sms - 1) / (8LL * sms);
+  const long long c = (want + 31) / 32 * 32;
+  return (int)std::min<long long>(kMaxChunk, std::max<long long>(kMinChunk, c));
 }
 
 int check(const snapkv_shape* sh, const int32_t* lens, int32_t layout, int32_t C) {
