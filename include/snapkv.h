@@ -292,6 +292,20 @@ int snapkv_decode_attention(const snapkv_shape *shape, const void *q, const void
                             int32_t C, float *out, void *workspace, size_t workspace_bytes,
                             void *stream);
 
+/*
+ * Self-test of the bounded device-side waits (the SnapKV pages have no
+ * counterpart; it lets the failure path be tested without faulting or
+ * hanging a GPU).  Enqueues one kernel whose single thread waits, with the
+ * same bounded wait the kernels use for their cross-CTA counters (2 s limit),
+ * on a device flag in workspace: set_flag = 0 leaves the flag unset, so the
+ * wait runs out and the status word becomes "timeout"; set_flag = 1 sets it
+ * first, so the wait succeeds.  Read the outcome with snapkv_get_status on
+ * the same workspace (SNAPKV_ERR_TIMEOUT or SNAPKV_OK).
+ *   workspace  device, 256-byte aligned, >= 512 bytes (overwritten).
+ * Returns SNAPKV_OK once enqueued, SNAPKV_ERR_INVALID_ARG, SNAPKV_ERR_CUDA.
+ */
+int snapkv_selftest_wait(void *workspace, size_t workspace_bytes, int32_t set_flag, void *stream);
+
 /* Static text for a status code. */
 const char *snapkv_status_string(int status);
 

@@ -43,6 +43,7 @@
 
 #include "plan.h"
 #include "tmem_ld.cuh"
+#include "wait.cuh"
 
 namespace snapkv {
 namespace tc {
@@ -58,7 +59,6 @@ constexpr int kGroupTiles = 1024;
 constexpr int kMergeRows = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSmemLimit = 232448;
-constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum : int { kP1 = 0, kMerge = 1, kP2 = 2, kDone = 3 };
@@ -108,22 +108,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
       : "memory");
   return done != 0;
 }
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-struct Ctl {
-  volatile int* abort;  // CTA-wide abort flag (shared memory)
-  int* status;          // device status word
-};
-
-__device__ __forceinline__ void raise_timeout(const Ctl& c) {
-  *c.abort = 1;
-  atomicExch(c.status, kDevTimeout);
-}
-
 // Bounded wait for the phase of parity `parity` of barrier b.  Returns false
 // when the CTA is aborting (flag already set, or this wait expired).  All of
 // it is inline: an out-of-line call on the MMA thread's per-tile path costs
@@ -146,21 +130,6 @@ __device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, const Ctl
   return mbar_test(b, parity) || wait_bar_slow(b, parity, c);
 }
 
-// Bounded wait until *ctr >= target (device-scope acquire).
-__device__ __forceinline__ bool wait_counter(const int* ctr, int target, const Ctl& c) {
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-    if (v >= target) return true;
-    if (*c.abort) return false;
-    if (global_ns() - t0 > kWaitNs) {
-      raise_timeout(c);
-      return false;
-    }
-    __nanosleep(128);
-  }
-}
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");

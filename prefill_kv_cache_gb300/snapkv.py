@@ -31,6 +31,7 @@ EXPORTED = (
     "snapkv_score_with_lse",
     "snapkv_decode_workspace_size",
     "snapkv_decode_attention",
+    "snapkv_selftest_wait",
     "snapkv_score_offsets",
     "snapkv_get_status",
     "snapkv_host_staging_size",
@@ -82,6 +83,8 @@ def load() -> ctypes.CDLL:
     lib.snapkv_decode_workspace_size.restype = sz
     lib.snapkv_decode_attention.argtypes = [shp, vp, vp, vp, i32, vp, i32, vp, vp, sz, vp]
     lib.snapkv_decode_attention.restype = ctypes.c_int
+    lib.snapkv_selftest_wait.argtypes = [vp, sz, i32, vp]
+    lib.snapkv_selftest_wait.restype = ctypes.c_int
     lib.snapkv_kernel_launches.argtypes = []
     lib.snapkv_kernel_launches.restype = ctypes.c_uint64
     lib.snapkv_score_offsets.argtypes = [shp, vp, i32, i32, ctypes.POINTER(sz),
@@ -380,3 +383,14 @@ def decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tens
     if rc:
         raise SnapKVError(rc, "snapkv_decode_attention")
     return out
+
+
+def selftest_wait(workspace: torch.Tensor, set_flag: bool, stream=None) -> int:
+    """snapkv_selftest_wait (include/snapkv.h), then snapkv_get_status: returns
+    SNAPKV_ERR_TIMEOUT when the flag was left unset, SNAPKV_OK otherwise."""
+    rc = load().snapkv_selftest_wait(workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(),
+                                     1 if set_flag else 0, _stream_handle(stream))
+    if rc:
+        raise SnapKVError(rc, "snapkv_selftest_wait")
+    return get_status(workspace, stream)

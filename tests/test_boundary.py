@@ -179,3 +179,10 @@ def test_decode_workspace():
     assert need > 0
     assert S.decode_workspace_size(sh, [1000, 5, 80000], S.CACHE_PACKED) >= need
     assert decode_rc(sh, [1000, 5, 70000], ws_bytes=need - 1) == S.ERR_WORKSPACE
+
+
+def test_selftest_wait_checks_arguments():
+    lib = S.load()
+    assert lib.snapkv_selftest_wait(None, 4096, 0, None) == S.ERR_INVALID_ARG
+    assert lib.snapkv_selftest_wait(FAKE, 256, 0, None) == S.ERR_INVALID_ARG
+    assert lib.snapkv_selftest_wait(FAKE + 16, 4096, 0, None) == S.ERR_INVALID_ARG
