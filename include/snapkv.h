@@ -137,6 +137,38 @@ int snapkv_score(const snapkv_shape *shape, const void *q_win, const void *k,
                  size_t workspace_bytes, void *stream);
 
 /*
+ * Selection variants (flags of the _ex entry points).
+ *
+ * SNAPKV_PER_QUERY_HEAD: every query head selects its own positions instead
+ * of one selection per KV head from the group-averaged score (the pages
+ * select "for each attention head": hotpaper.ai summary of "SnapKV: LLM
+ * Knows What You are Looking for Before Generation", abstract; GQA support,
+ * glossary "SnapKV" FAQ Q1).  Query head hq's raw score is its own window
+ * sum, without the 1/g mean; pooling and selection are per query head, and
+ * query head hq gathers the K and V rows of KV head hq / g.  The outputs then
+ * have H_q heads: out_k, out_v [B, C, H_q, d], out_idx [B, H_q, C], and the
+ * fp32 score vectors hold H_q * P_b values per sequence, packed (b, hq, j).
+ * Needs g = H_q / H_kv <= 8 (else SNAPKV_ERR_UNSUPPORTED).  With g = 1 it is
+ * exactly snapkv_compress.
+ */
+#define SNAPKV_PER_QUERY_HEAD 1
+
+size_t snapkv_workspace_size_ex(const snapkv_shape *shape, const int32_t *seqlens_host,
+                                int32_t W, int32_t C, int32_t flags);
+
+int snapkv_score_offsets_ex(const snapkv_shape *shape, const int32_t *seqlens_host, int32_t W,
+                            int32_t C, int32_t flags, size_t *raw_offset,
+                            size_t *pooled_offset, size_t *count);
+
+/* snapkv_compress with flags (0 = snapkv_compress).  Unknown flags are
+ * SNAPKV_ERR_INVALID_ARG. */
+int snapkv_compress_ex(const snapkv_shape *shape, const void *q_win, const void *k,
+                       const void *v, const int32_t *seqlens_host, int32_t W,
+                       int32_t kernel_size, int32_t pool_type, int32_t C, void *out_k,
+                       void *out_v, int32_t *out_idx, void *workspace, size_t workspace_bytes,
+                       void *stream, int32_t flags);
+
+/*
  * snapkv_compress and snapkv_score with the window rows' log-sum-exp given
  * by the caller.  The prefill attention that precedes SnapKV already
  * normalises every window query row over its causally visible keys (the

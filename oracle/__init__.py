@@ -170,3 +170,17 @@ def compress(q_win, k, v, seqlens, W: int, k_pool: int, pool_type, C: int,
         pooleds.append(pooled[o:o + H_kv * P].reshape(H_kv, P))
     return dict(raw=raws, pooled=pooleds, tau=tau.reshape(B, H_kv),
                 window_mass=wm.reshape(B, H_kv), idx=idx, out_k=out_k, out_v=out_v)
+
+
+def compress_per_q_head(q_win, k, v, seqlens, W: int, k_pool: int, pool_type, C: int,
+                        nthreads=None):
+    """Per-query-head selection: every query head hq scores (its own window
+    sum, no group mean), pools and selects on its own over the rows of KV
+    head hq // g (the pages select "for each attention head": hotpaper.ai
+    summary, abstract).  That is the group-averaged compression of an MHA
+    layer whose KV head hq is a copy of KV head hq // g, since a group of one
+    query head has the identity as its mean; the outputs have H_q heads."""
+    g = q_win.shape[2] // k.shape[1]
+    kx = np.ascontiguousarray(np.repeat(k, g, axis=1))
+    vx = np.ascontiguousarray(np.repeat(v, g, axis=1))
+    return compress(q_win, kx, vx, seqlens, W, k_pool, pool_type, C, nthreads=nthreads)

@@ -53,6 +53,10 @@ struct Plan {
   float2* stats;     // [total_pieces * Wp] (running max, sum of exp) per piece and row
   float* lse;        // [nseq * H_kv * Wp] natural-log LSE per (sequence, head, row)
   const float* lse_in;  // caller's window LSE [B, W, H_q] (natural log), or null
+  // output heads: H_kv (scores averaged over each KV head's query group), or
+  // H_q when every query head selects for itself (head_div = g: output head
+  // o gathers KV head o / head_div)
+  int out_heads, head_div;
   int* status;       // device status word
   int* counters;     // work-queue head and per-group completion counters
   long long total_rows;  // rows of k / v in the whole call (T)

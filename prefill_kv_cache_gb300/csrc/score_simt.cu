@@ -171,6 +171,32 @@ score_pass2_simt(const __grid_constant__ Plan p) {
   __syncthreads();
 
   const T* kbase = static_cast<const T*>(p.k);
+  if (p.out_heads != p.H_kv) {
+    // every query head keeps its own sum (member m = row % g), no group mean
+    float* rawq = p.raw + S.score0 + (size_t)h * p.g * S.P;
+    for (int j = key_begin + threadIdx.x; j < key_end; j += blockDim.x) {
+      float kr[D];
+      const T* kp = kbase + ((size_t)(S.row0 + j) * p.H_kv + h) * D;
+#pragma unroll
+      for (int e = 0; e < D; ++e) kr[e] = to_f(kp[e]);
+      float accm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int row = 0; row < p.Wp; ++row) {
+        const T* qr = qs + (size_t)row * D;
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < D; ++e) dot = fmaf(to_f(qr[e]), kr[e], dot);
+        const float v = expf(dot * p.scale - lse_s[row]);
+        const int m = row % p.g;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k == m) accm[k] += v;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k < p.g) rawq[(size_t)k * S.P + j] = accm[k];
+    }
+    return;
+  }
   float* raw = p.raw + S.score0 + (size_t)h * S.P;
   for (int j = key_begin + threadIdx.x; j < key_end; j += blockDim.x) {
     float kr[D];

@@ -212,6 +212,23 @@ __device__ __forceinline__ float row_sum(const float* v, const float* lse2, floa
   return (a0 + a1) + (a2 + a3);
 }
 
+// As row_sum, keeping 8 partial sums by column index mod 8 (the query-head
+// member of a row when the group size divides 8).
+template <int N>
+__device__ __forceinline__ void row_sum_members(const float* v, const float* lse2, float c2,
+                                                float (&a)[8]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = 0.f;
+#pragma unroll
+  for (int j = 0; j < N; j += 4) {
+    const float4 m4 = *reinterpret_cast<const float4*>(lse2 + j);
+    a[j & 7] += ex2(fmaf(v[j], c2, -m4.x));
+    a[(j + 1) & 7] += ex2(fmaf(v[j + 1], c2, -m4.y));
+    a[(j + 2) & 7] += ex2(fmaf(v[j + 2], c2, -m4.z));
+    a[(j + 3) & 7] += ex2(fmaf(v[j + 3], c2, -m4.w));
+  }
+}
+
 // ------------------------------------------------------------ schedule ---
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -264,6 +281,8 @@ __device__ Entry decode(const Plan& p, const TcPlan& tp, int idx) {
 
 // ---------------------------------------------------------- the kernel ---
 
+// PER_Q: every query head keeps its own pass-2 sums (per-query-head selection)
+template <bool PER_Q>
 __global__ void __launch_bounds__(kThreads, 1)
 score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan tp,
                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q) {
@@ -649,6 +668,26 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
               Mrow[rb] = Mn;
             }
           }
+        } else if (PER_Q) {
+          // every query head keeps its own sum: member m of the group owns
+          // the rows r with r % g == m; the two groups' halves add up in the
+          // zeroed score array (two addends onto zero: order-independent)
+          float am[8];
+          if (wp == 256)
+            row_sum_members<128>(s, aux + wg * 128, c2, am);
+          else
+            row_sum_members<64>(s, aux + wg * 64, c2, am);
+          const int key = key0 + lrow;
+          if (key < S.P) {
+            float* base = p.raw + S.score0 + (size_t)h * p.g * S.P + key;
+            for (int m = 0; m < p.g; ++m) {
+              float v = 0.f;
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                if (k % p.g == m) v += am[k];
+              atomicAdd(base + (size_t)m * S.P, v);
+            }
+          }
         } else {
           const float acc = wp == 256 ? row_sum<128>(s, aux + wg * 128, c2)
                                       : row_sum<64>(s, aux + wg * 64, c2);
@@ -845,14 +884,28 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken) {
   if (!make_map(&tm_q, p.q, p.d, p.H_q, (long long)p.batch * p.W, p.g, p.W)) return cudaSuccess;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaFuncSetAttribute(score_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = p.out_heads != p.H_kv ? score_tc_kernel<true> : score_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   // zero the queue head and the per-group counters
   e = cudaMemsetAsync(p.counters, 0, sizeof(int) * (1 + 2 * g), st);
   if (e != cudaSuccess) return e;
+  if (p.out_heads != p.H_kv) {  // per-query-head scores are added up by the two consumer groups
+    long long lo = -1, hi = 0;
+    for (int s = 0; s < p.nseq; ++s) {
+      const SeqInfo& S = p.seq[s];
+      if (!S.scored) continue;
+      if (lo < 0) lo = S.score0;
+      hi = S.score0 + (long long)p.out_heads * S.P;
+    }
+    if (hi > lo && lo >= 0) {
+      e = cudaMemsetAsync(p.raw + lo, 0, sizeof(float) * (size_t)(hi - lo), st);
+      if (e != cudaSuccess) return e;
+    }
+  }
   const int grid = sms < tp.total_items ? sms : tp.total_items;
-  score_tc_kernel<<<grid, kThreads, smem, st>>>(p, tp, tm_k, tm_q);
+  kern<<<grid, kThreads, smem, st>>>(p, tp, tm_k, tm_q);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   count_launches(1);

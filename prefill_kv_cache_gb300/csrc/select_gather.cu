@@ -131,9 +131,9 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
   return before + x - v;
 }
 
-// Copy `cnt` rows: source position pos[i] of the sequence -> output slot
-// slot0 + i, K and V, 16 B per access.
-__device__ __forceinline__ void copy_rows(const Plan& p, const SeqInfo& S, int h,
+// Copy `cnt` rows: source position pos[i] of the sequence (KV head sh) ->
+// output slot slot0 + i (output head oh), K and V, 16 B per access.
+__device__ __forceinline__ void copy_rows(const Plan& p, const SeqInfo& S, int sh, int oh,
                                           const int* pos, int cnt, int slot0, int vecs) {
   const uint4* kin = static_cast<const uint4*>(p.k);
   const uint4* vin = static_cast<const uint4*>(p.v);
@@ -150,8 +150,8 @@ __device__ __forceinline__ void copy_rows(const Plan& p, const SeqInfo& S, int h
       const int e = e0 + u * blockDim.x;
       if (e < total) {
         const int it = e / vecs, vv = e % vecs;
-        const size_t src = ((size_t)(S.row0 + pos[it]) * p.H_kv + h) * vecs + vv;
-        dst[u] = (((size_t)S.b * p.C + slot0 + it) * p.H_kv + h) * vecs + vv;
+        const size_t src = ((size_t)(S.row0 + pos[it]) * p.H_kv + sh) * vecs + vv;
+        dst[u] = (((size_t)S.b * p.C + slot0 + it) * p.out_heads + oh) * vecs + vv;
         kv[u] = __ldcs(kin + src);
         vv_[u] = __ldcs(vin + src);
       }
@@ -195,11 +195,11 @@ __device__ bool bar_wait(uint64_t* b, uint32_t parity, int* status) {
   }
 }
 
-// Copies the K and V rows of sequence positions pos[0..cnt) (KV head h) to
-// output slots slot0.. : batches of rows are fetched into `stage` by bulk
+// Copies the K and V rows of sequence positions pos[0..cnt) (KV head sh) to
+// output slots slot0.. of output head oh: batches of rows are fetched into `stage` by bulk
 // copies that complete on `bar`, then written out by bulk stores.  Every
 // thread of the block calls it.  False if a wait expired.
-__device__ bool bulk_copy_rows(const Plan& p, const SeqInfo& S, int h, const int* pos, int cnt,
+__device__ bool bulk_copy_rows(const Plan& p, const SeqInfo& S, int sh, int oh, const int* pos, int cnt,
                                int slot0, int row_bytes, unsigned char* stage, int stage_bytes,
                                uint64_t* bar, uint32_t& phase) {
   const int per = stage_bytes / (2 * row_bytes);  // rows per batch (K and V)
@@ -221,7 +221,7 @@ __device__ bool bulk_copy_rows(const Plan& p, const SeqInfo& S, int h, const int
     for (int i = threadIdx.x; i < 2 * m; i += blockDim.x) {
       const int row = i >> 1;
       const char* src = ((i & 1) ? vin : kin) +
-                        ((size_t)(S.row0 + pos[i0 + row]) * p.H_kv + h) * row_bytes;
+                        ((size_t)(S.row0 + pos[i0 + row]) * p.H_kv + sh) * row_bytes;
       asm volatile(
           "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
               "r"(saddr(stage + (size_t)i * row_bytes)),
@@ -238,7 +238,7 @@ __device__ bool bulk_copy_rows(const Plan& p, const SeqInfo& S, int h, const int
       for (int i = threadIdx.x; i < 2 * m; i += blockDim.x) {
         const int row = i >> 1;
         char* dst = ((i & 1) ? vout : kout) +
-                    (((size_t)S.b * p.C + slot0 + i0 + row) * p.H_kv + h) * row_bytes;
+                    (((size_t)S.b * p.C + slot0 + i0 + row) * p.out_heads + oh) * row_bytes;
         asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
                      "r"(saddr(stage + (size_t)i * row_bytes)), "r"(row_bytes)
                      : "memory");
@@ -269,7 +269,8 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
   const int CS = (int)cluster.num_blocks();
   const int t = threadIdx.x;
   const int unit = blockIdx.y;
-  const int s = unit / p.H_kv, h = unit % p.H_kv;
+  const int s = unit / p.out_heads, oh = unit % p.out_heads;  // output head
+  const int h = oh / p.head_div;                                // its KV head
   const SeqInfo& S = p.seq[s];
   const int vecs = p.d * (p.dtype == 0 ? 2 : 4) / 16;
   const int row_bytes = vecs * 16;
@@ -279,7 +280,7 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  int32_t* idx_out = p.out_idx + ((size_t)S.b * p.H_kv + h) * p.C;
+  int32_t* idx_out = p.out_idx + ((size_t)S.b * p.out_heads + oh) * p.C;
 
   if (!S.scored) {
     // L <= C: slots 0..L-1 take positions 0..L-1, the rest index -1 and zeros.
@@ -292,7 +293,7 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
     const uint4* vin = static_cast<const uint4*>(p.v);
     for (int x = t; x < (e - a) * vecs; x += blockDim.x) {
       const int slot = a + x / vecs, vv = x % vecs;
-      const size_t dst = (((size_t)S.b * p.C + slot) * p.H_kv + h) * vecs + vv;
+      const size_t dst = (((size_t)S.b * p.C + slot) * p.out_heads + oh) * vecs + vv;
       if (slot < S.L) {
         const size_t src = ((size_t)(S.row0 + slot) * p.H_kv + h) * vecs + vv;
         kout[dst] = __ldcs(kin + src);
@@ -309,8 +310,8 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
   const int Sz = (P + CS - 1) / CS;
   const int j0 = min(P, rank * Sz), j1 = min(P, j0 + Sz);
   const int cnt = j1 - j0;
-  const float* raw = p.raw + S.score0 + (size_t)h * P;
-  float* pooled = p.pooled + S.score0 + (size_t)h * P;
+  const float* raw = p.raw + S.score0 + (size_t)oh * P;
+  float* pooled = p.pooled + S.score0 + (size_t)oh * P;
   const bool in_smem = raw_span(r) + cnt <= cap_floats;
   float* sraw = dyn;
   float* spool = dyn + raw_span(r);
@@ -519,11 +520,11 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
     for (int i = t; i < m; i += blockDim.x) sel_pos[i] = __ldcg(idx_out + c0 + i);
     __syncthreads();
     if (bulk) {
-      if (!bulk_copy_rows(p, S, h, sel_pos, m, c0, row_bytes, reinterpret_cast<unsigned char*>(dyn),
+      if (!bulk_copy_rows(p, S, h, oh, sel_pos, m, c0, row_bytes, reinterpret_cast<unsigned char*>(dyn),
                           cap_floats * 4, &bulk_bar, bulk_phase))
         break;
     } else {
-      copy_rows(p, S, h, sel_pos, m, c0, vecs);
+      copy_rows(p, S, h, oh, sel_pos, m, c0, vecs);
     }
   }
 }
@@ -582,7 +583,7 @@ int launch_select_gather(const Plan& p, void* stream) {
   // Cluster size: a power of two, large enough that all units together fill
   // the GPU and each slice fits the shared-memory staging, then halved while
   // the clusters would not all be resident at once (one wave).
-  const int units = p.nseq * p.H_kv;
+  const int units = p.nseq * p.out_heads;
   int maxP = 0;
   for (int s = 0; s < p.nseq; ++s)
     if (p.seq[s].scored) maxP = max(maxP, p.seq[s].P);

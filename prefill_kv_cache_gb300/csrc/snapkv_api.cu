@@ -51,9 +51,21 @@ int check_problem(const snapkv_shape* sh, const int32_t* seqlens, int W, int C) 
   return SNAPKV_OK;
 }
 
+// Flags of the _ex entry points: known bits only; per-query-head selection
+// needs groups of at most 8 query heads.
+int check_flags(const snapkv_shape* sh, int32_t flags) {
+  if (!sh) return SNAPKV_ERR_INVALID_ARG;
+  if (flags & ~SNAPKV_PER_QUERY_HEAD) return SNAPKV_ERR_INVALID_ARG;
+  if ((flags & SNAPKV_PER_QUERY_HEAD) && sh->num_kv_heads > 0 &&
+      sh->num_q_heads / sh->num_kv_heads > 8)
+    return SNAPKV_ERR_UNSUPPORTED;
+  return SNAPKV_OK;
+}
+
 int chunks_for(int L) { return (L + kChunkKeys - 1) / kChunkKeys; }
 
-Layout layout_for(const snapkv_shape* sh, const int32_t* seqlens, int W, int C) {
+Layout layout_for(const snapkv_shape* sh, const int32_t* seqlens, int W, int C,
+                  bool per_q = false) {
   Layout lay;
   const int H = sh->num_kv_heads;
   const int Wp = W * (sh->num_q_heads / H);
@@ -63,7 +75,7 @@ Layout layout_for(const snapkv_shape* sh, const int32_t* seqlens, int W, int C) 
     size_t pieces = 0;
     for (int b = g0; b < g1; ++b) {
       if (seqlens[b] > C) {
-        scores += (size_t)H * (seqlens[b] - W);
+        scores += (size_t)(per_q ? sh->num_q_heads : H) * (seqlens[b] - W);
         pieces += (size_t)H * chunks_for(seqlens[b]);
       }
     }
@@ -117,12 +129,27 @@ size_t snapkv_workspace_size(const snapkv_shape* shape, const int32_t* seqlens_h
   return layout_for(shape, seqlens_host, W, C).total;
 }
 
+size_t snapkv_workspace_size_ex(const snapkv_shape* shape, const int32_t* seqlens_host,
+                                int32_t W, int32_t C, int32_t flags) {
+  if (check_flags(shape, flags) != SNAPKV_OK) return 0;
+  if (check_problem(shape, seqlens_host, W, C) != SNAPKV_OK) return 0;
+  return layout_for(shape, seqlens_host, W, C, flags & SNAPKV_PER_QUERY_HEAD).total;
+}
+
 int snapkv_score_offsets(const snapkv_shape* shape, const int32_t* seqlens_host, int32_t W,
                          int32_t C, size_t* raw_offset, size_t* pooled_offset, size_t* count) {
-  const int rc = check_problem(shape, seqlens_host, W, C);
+  return snapkv_score_offsets_ex(shape, seqlens_host, W, C, 0, raw_offset, pooled_offset, count);
+}
+
+int snapkv_score_offsets_ex(const snapkv_shape* shape, const int32_t* seqlens_host, int32_t W,
+                            int32_t C, int32_t flags, size_t* raw_offset, size_t* pooled_offset,
+                            size_t* count) {
+  int rc = check_flags(shape, flags);
+  if (rc != SNAPKV_OK) return rc;
+  rc = check_problem(shape, seqlens_host, W, C);
   if (rc != SNAPKV_OK) return rc;
   if (!raw_offset || !pooled_offset || !count) return SNAPKV_ERR_INVALID_ARG;
-  const Layout lay = layout_for(shape, seqlens_host, W, C);
+  const Layout lay = layout_for(shape, seqlens_host, W, C, flags & SNAPKV_PER_QUERY_HEAD);
   *raw_offset = lay.raw;
   *pooled_offset = lay.pooled;
   *count = lay.score_count;
@@ -135,7 +162,8 @@ namespace {
 int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const void* v,
             const int32_t* seqlens_host, int32_t W, int32_t kernel_size, int32_t pool_type,
             int32_t C, void* out_k, void* out_v, int32_t* out_idx, void* workspace,
-            size_t workspace_bytes, void* stream, bool score_only, const float* lse_in) {
+            size_t workspace_bytes, void* stream, bool score_only, const float* lse_in,
+            bool per_q = false) {
   int rc = check_problem(shape, seqlens_host, W, C);
   if (rc == SNAPKV_ERR_INVALID_ARG) return rc;
   if (!q_win || !k || !workspace) return SNAPKV_ERR_INVALID_ARG;
@@ -150,7 +178,7 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
       return SNAPKV_ERR_INVALID_ARG;
   }
   if (rc != SNAPKV_OK) return rc;
-  const Layout lay = layout_for(shape, seqlens_host, W, C);
+  const Layout lay = layout_for(shape, seqlens_host, W, C, per_q);
   if (workspace_bytes < lay.total) return SNAPKV_ERR_WORKSPACE;
 
   char* ws = static_cast<char*>(workspace);
@@ -185,6 +213,8 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
   p.stats = reinterpret_cast<float2*>(ws + lay.stats);
   p.lse = reinterpret_cast<float*>(ws + lay.lse);
   p.lse_in = lse_in;
+  p.out_heads = per_q ? p.H_q : H;
+  p.head_div = per_q ? p.g : 1;
   p.status = reinterpret_cast<int*>(ws + lay.status);
   p.counters = reinterpret_cast<int*>(ws + lay.counters);
   p.batch = shape->batch;
@@ -207,7 +237,7 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
       S.piece0 = piece;
       S.chunks = S.scored ? chunks_for(S.L) : 0;
       piece += S.chunks * H;
-      if (S.scored) score0 += (long long)H * S.P;
+      if (S.scored) score0 += (long long)p.out_heads * S.P;
       row0 += S.L;
     }
     p.total_pieces = piece;
@@ -236,6 +266,17 @@ int snapkv_score(const snapkv_shape* shape, const void* q_win, const void* k,
                  size_t workspace_bytes, void* stream) {
   return enqueue(shape, q_win, k, nullptr, seqlens_host, W, 1, SNAPKV_POOL_AVG, C, nullptr,
                  nullptr, nullptr, workspace, workspace_bytes, stream, true, nullptr);
+}
+
+int snapkv_compress_ex(const snapkv_shape* shape, const void* q_win, const void* k, const void* v,
+                       const int32_t* seqlens_host, int32_t W, int32_t kernel_size,
+                       int32_t pool_type, int32_t C, void* out_k, void* out_v, int32_t* out_idx,
+                       void* workspace, size_t workspace_bytes, void* stream, int32_t flags) {
+  const int rc = check_flags(shape, flags);
+  if (rc != SNAPKV_OK) return rc;
+  return enqueue(shape, q_win, k, v, seqlens_host, W, kernel_size, pool_type, C, out_k, out_v,
+                 out_idx, workspace, workspace_bytes, stream, false, nullptr,
+                 (flags & SNAPKV_PER_QUERY_HEAD) != 0);
 }
 
 int snapkv_compress_with_lse(const snapkv_shape* shape, const void* q_win, const void* k,

@@ -32,6 +32,9 @@ EXPORTED = (
     "snapkv_decode_workspace_size",
     "snapkv_decode_attention",
     "snapkv_selftest_wait",
+    "snapkv_workspace_size_ex",
+    "snapkv_score_offsets_ex",
+    "snapkv_compress_ex",
     "snapkv_score_offsets",
     "snapkv_get_status",
     "snapkv_host_staging_size",
@@ -85,6 +88,14 @@ def load() -> ctypes.CDLL:
     lib.snapkv_decode_attention.restype = ctypes.c_int
     lib.snapkv_selftest_wait.argtypes = [vp, sz, i32, vp]
     lib.snapkv_selftest_wait.restype = ctypes.c_int
+    lib.snapkv_workspace_size_ex.argtypes = [shp, vp, i32, i32, i32]
+    lib.snapkv_workspace_size_ex.restype = sz
+    lib.snapkv_score_offsets_ex.argtypes = [shp, vp, i32, i32, i32, ctypes.POINTER(sz),
+                                            ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    lib.snapkv_score_offsets_ex.restype = ctypes.c_int
+    lib.snapkv_compress_ex.argtypes = [shp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp,
+                                       sz, vp, i32]
+    lib.snapkv_compress_ex.restype = ctypes.c_int
     lib.snapkv_kernel_launches.argtypes = []
     lib.snapkv_kernel_launches.restype = ctypes.c_uint64
     lib.snapkv_score_offsets.argtypes = [shp, vp, i32, i32, ctypes.POINTER(sz),
@@ -148,18 +159,26 @@ def make_shape(batch, num_q_heads, num_kv_heads, head_dim, dtype) -> snapkv_shap
                         dtype if isinstance(dtype, int) else dtype_code(dtype))
 
 
-def workspace_size(shape: snapkv_shape, seqlens, window_size: int, max_capacity_prompt: int) -> int:
+PER_QUERY_HEAD = 1  # flag of the _ex entry points (include/snapkv.h)
+
+
+def workspace_size(shape: snapkv_shape, seqlens, window_size: int, max_capacity_prompt: int,
+                   flags: int = 0) -> int:
     arr, _ = _seqlens_array(seqlens)
+    if flags:
+        return int(load().snapkv_workspace_size_ex(ctypes.byref(shape), arr, int(window_size),
+                                                   int(max_capacity_prompt), int(flags)))
     return int(load().snapkv_workspace_size(ctypes.byref(shape), arr, int(window_size),
                                             int(max_capacity_prompt)))
 
 
-def score_offsets(shape: snapkv_shape, seqlens, window_size: int, max_capacity_prompt: int):
+def score_offsets(shape: snapkv_shape, seqlens, window_size: int, max_capacity_prompt: int,
+                  flags: int = 0):
     arr, _ = _seqlens_array(seqlens)
     r, p, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
-    rc = load().snapkv_score_offsets(ctypes.byref(shape), arr, int(window_size),
-                                     int(max_capacity_prompt), ctypes.byref(r), ctypes.byref(p),
-                                     ctypes.byref(c))
+    rc = load().snapkv_score_offsets_ex(ctypes.byref(shape), arr, int(window_size),
+                                        int(max_capacity_prompt), int(flags), ctypes.byref(r),
+                                        ctypes.byref(p), ctypes.byref(c))
     if rc:
         raise SnapKVError(rc, "snapkv_score_offsets")
     return r.value, p.value, c.value
@@ -175,14 +194,15 @@ def compress(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seqlens,
              window_size: int, kernel_size: int, pooling, max_capacity_prompt: int,
              out_k: torch.Tensor | None = None, out_v: torch.Tensor | None = None,
              out_idx: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-             stream=None, lse_win: torch.Tensor | None = None):
+             stream=None, lse_win: torch.Tensor | None = None, flags: int = 0):
     """Compress one layer (see include/snapkv.h, snapkv_compress).
 
     q_win [B, W, H_q, d], k / v [T, H_kv, d] (packed, bf16 or fp32, CUDA);
     seqlens: B host integers.  Returns (out_k, out_v, out_idx, workspace);
     outputs that are not given are allocated here with torch.  With lse_win
     (fp32 [B, W, H_q], the window rows' natural-log LSE) the call goes to
-    snapkv_compress_with_lse.
+    snapkv_compress_with_lse; with flags (PER_QUERY_HEAD) to snapkv_compress_ex,
+    whose outputs have H_q heads.
     """
     B, W, H_q, d = q_win.shape
     H_kv = k.shape[1]
@@ -190,13 +210,16 @@ def compress(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seqlens,
     if W != int(window_size):
         raise ValueError("q_win's second dimension must equal window_size")
     shape = make_shape(B, H_q, H_kv, d, q_win.dtype)
+    H_out = H_q if flags & PER_QUERY_HEAD else H_kv
+    if lse_win is not None and flags:
+        raise ValueError("lse_win and flags cannot be combined")
     if out_k is None:
-        out_k = torch.empty((B, C, H_kv, d), dtype=k.dtype, device=k.device)
+        out_k = torch.empty((B, C, H_out, d), dtype=k.dtype, device=k.device)
     if out_v is None:
-        out_v = torch.empty((B, C, H_kv, d), dtype=k.dtype, device=k.device)
+        out_v = torch.empty((B, C, H_out, d), dtype=k.dtype, device=k.device)
     if out_idx is None:
-        out_idx = torch.empty((B, H_kv, C), dtype=torch.int32, device=k.device)
-    ws_bytes = workspace_size(shape, seqlens, W, C)
+        out_idx = torch.empty((B, H_out, C), dtype=torch.int32, device=k.device)
+    ws_bytes = workspace_size(shape, seqlens, W, C, flags)
     if ws_bytes == 0:
         raise SnapKVError(ERR_INVALID_ARG, "snapkv_workspace_size")
     if workspace is None:
@@ -210,7 +233,13 @@ def compress(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seqlens,
         _check_lse(lse_win, B, W, H_q)
     ws_args = (workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                _stream_handle(stream))
-    if lse_win is None:
+    if flags:
+        rc = load().snapkv_compress_ex(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(),
+                                       v.data_ptr(), arr, W, int(kernel_size), pool_code(pooling),
+                                       C, out_k.data_ptr(), out_v.data_ptr(), out_idx.data_ptr(),
+                                       *ws_args, int(flags))
+        name = "snapkv_compress_ex"
+    elif lse_win is None:
         rc = load().snapkv_compress(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(),
                                     v.data_ptr(), arr, W, int(kernel_size), pool_code(pooling), C,
                                     out_k.data_ptr(), out_v.data_ptr(), out_idx.data_ptr(),
@@ -284,9 +313,9 @@ def get_status(workspace: torch.Tensor, stream=None) -> int:
 
 
 def scores_from_workspace(workspace: torch.Tensor, shape: snapkv_shape, seqlens,
-                          window_size: int, max_capacity_prompt: int):
+                          window_size: int, max_capacity_prompt: int, flags: int = 0):
     """(raw, pooled) fp32 views into the workspace after a compress call."""
-    r, p, c = score_offsets(shape, seqlens, window_size, max_capacity_prompt)
+    r, p, c = score_offsets(shape, seqlens, window_size, max_capacity_prompt, flags)
     raw = workspace[r:r + 4 * c].view(torch.float32)
     pooled = workspace[p:p + 4 * c].view(torch.float32)
     return raw, pooled

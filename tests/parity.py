@@ -60,18 +60,20 @@ def window_lse(lay, C, fill=np.nan):
     return out
 
 
-def run_gpu(lay, k_pool, pool, C, dev="cuda", lse=None):
-    """One snapkv_compress (snapkv_compress_with_lse when `lse` is given) on
-    the layer; returns numpy outputs and scores."""
+def run_gpu(lay, k_pool, pool, C, dev="cuda", lse=None, flags=0):
+    """One snapkv_compress (snapkv_compress_with_lse when `lse` is given,
+    snapkv_compress_ex when flags are) on the layer; returns numpy outputs
+    and scores."""
     q = to_device(lay.q_win, dev)
     k = to_device(lay.k, dev)
     v = to_device(lay.v, dev)
     lse_t = None if lse is None else to_device(lse, dev)
-    ok, ov, oi, ws = S.compress(q, k, v, lay.seqlens, lay.W, k_pool, pool, C, lse_win=lse_t)
+    ok, ov, oi, ws = S.compress(q, k, v, lay.seqlens, lay.W, k_pool, pool, C, lse_win=lse_t,
+                                flags=flags)
     st = S.get_status(ws)
     assert st == S.OK, S.status_string(st)
     shape = S.make_shape(lay.B, lay.H_q, lay.H_kv, lay.d, q.dtype)
-    raw, pooled = S.scores_from_workspace(ws, shape, lay.seqlens, lay.W, C)
+    raw, pooled = S.scores_from_workspace(ws, shape, lay.seqlens, lay.W, C, flags)
     torch.cuda.synchronize()
 
     def host(t):
@@ -158,3 +160,15 @@ def oracle_for(lay, k_pool, pool, C, seqs=None, nthreads=None):
     vs = np.concatenate([lay.v[offs[b]:offs[b] + lay.seqlens[b]] for b in seqs])
     sl = [int(lay.seqlens[b]) for b in seqs]
     return oracle.compress(q, ks, vs, sl, lay.W, k_pool, pool, C, nthreads=nthreads)
+
+
+def expand_heads(lay):
+    """The layer with each KV head repeated for the g query heads it serves
+    (H_kv := H_q): per-query-head selection on `lay` equals the plain
+    compression of this layer."""
+    import dataclasses
+    g = lay.H_q // lay.H_kv
+    return dataclasses.replace(lay, k=np.ascontiguousarray(np.repeat(lay.k, g, axis=1)),
+                               v=np.ascontiguousarray(np.repeat(lay.v, g, axis=1)),
+                               H_kv=lay.H_q,
+                               targets=[[t[h // g] for h in range(lay.H_q)] for t in lay.targets])

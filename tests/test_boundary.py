@@ -186,3 +186,24 @@ def test_selftest_wait_checks_arguments():
     assert lib.snapkv_selftest_wait(None, 4096, 0, None) == S.ERR_INVALID_ARG
     assert lib.snapkv_selftest_wait(FAKE, 256, 0, None) == S.ERR_INVALID_ARG
     assert lib.snapkv_selftest_wait(FAKE + 16, 4096, 0, None) == S.ERR_INVALID_ARG
+
+
+def test_compress_ex_flags():
+    lib = S.load()
+    arr = (ctypes.c_int32 * 1)(4096)
+
+    def rc(flags, sh):
+        return lib.snapkv_compress_ex(ctypes.byref(sh), FAKE, FAKE, FAKE, arr, 32, 5, 0, 1024,
+                                      FAKE, FAKE, FAKE, FAKE, 1 << 30, None, flags)
+    assert rc(2, shape()) == S.ERR_INVALID_ARG
+    assert rc(S.PER_QUERY_HEAD, shape(Hq=32, Hkv=2)) == S.ERR_UNSUPPORTED  # group of 16
+    assert rc(S.PER_QUERY_HEAD, shape(d=96)) == S.ERR_UNSUPPORTED
+    sh = shape(Hq=32, Hkv=8)
+    plain = S.workspace_size(sh, [20000], 32, 1024)
+    per_q = S.workspace_size(sh, [20000], 32, 1024, S.PER_QUERY_HEAD)
+    assert per_q > plain  # four times the score vectors
+    assert S.workspace_size(shape(Hq=8, Hkv=8), [20000], 32, 1024, S.PER_QUERY_HEAD) == \
+        S.workspace_size(shape(Hq=8, Hkv=8), [20000], 32, 1024)
+    r0, p0, c0 = S.score_offsets(sh, [20000], 32, 1024)
+    r1, p1, c1 = S.score_offsets(sh, [20000], 32, 1024, S.PER_QUERY_HEAD)
+    assert c1 == 4 * c0

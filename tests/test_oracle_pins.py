@@ -347,3 +347,30 @@ def test_page_parameters_and_workloads_in_range():
         assert pp["window_size_range"]["min"] <= cfg["W"] <= pp["window_size_range"]["max"]
         assert cfg["k_pool"] % 2 == 1
         assert cfg["pool"] + "pool" in pp["pooling_types"]["values"]
+
+
+# ---- per-query-head selection (SNAPKV_PER_QUERY_HEAD) ----
+
+def test_per_q_head_with_groups_of_one_is_the_plain_compression():
+    lay = synth.make_inputs(21, [300, 90], 4, 4, 64, 16, "bf16", nspans=2)
+    a = oracle.compress(lay.q_win, lay.k, lay.v, lay.seqlens, lay.W, 5, "avg", 128)
+    b = oracle.compress_per_q_head(lay.q_win, lay.k, lay.v, lay.seqlens, lay.W, 5, "avg", 128)
+    np.testing.assert_array_equal(a["idx"], b["idx"])
+    np.testing.assert_array_equal(a["out_k"], b["out_k"])
+
+
+def test_per_q_head_scores_average_to_the_group_score():
+    """The g query heads' own raw scores average to their KV head's score."""
+    lay = synth.make_inputs(22, [400], 8, 2, 64, 16, "bf16", nspans=2)
+    C = 128
+    a = oracle.compress(lay.q_win, lay.k, lay.v, lay.seqlens, lay.W, 5, "max", C)
+    b = oracle.compress_per_q_head(lay.q_win, lay.k, lay.v, lay.seqlens, lay.W, 5, "max", C)
+    g = 4
+    for h in range(2):
+        mean = np.mean([b["raw"][0][h * g + m] for m in range(g)], axis=0)
+        np.testing.assert_allclose(mean, a["raw"][0][h], rtol=1e-12, atol=1e-15)
+    # each query head keeps positions of its own KV head's rows
+    assert b["idx"].shape == (1, 8, C)
+    for hq in range(8):
+        rows = b["idx"][0, hq]
+        np.testing.assert_array_equal(b["out_k"][0, :, hq], lay.k[rows, hq // g])
