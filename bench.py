@@ -278,13 +278,8 @@ def main():
     sampler.stop()
     launches = S.kernel_launches() - n0
     barrier()
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens_per_step = sum(seqlens) * layers
-    value = tokens_per_step * world / (ms / 1e3)
+    ms = replica_ms(e0.elapsed_time(e1) / args.steps, world, dev)
+    value = replica_value(sum(seqlens) * layers, world, ms)
 
     # score kernel alone, per launch, on the launching stream
     score_ms = []
@@ -355,6 +350,26 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def replica_ms(ms_local: float, world: int, dev) -> float:
+    """Step time of the whole job: the slowest replica's (max over ranks).
+    The replicas share nothing on the data path: this reduction and the
+    barriers around the timed region are the only collectives."""
+    if world <= 1:
+        return ms_local
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(tokens_per_step_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank compresses its own layers (weak
+    scaling), all ranks' tokens over the slowest rank's time."""
+    return tokens_per_step_per_rank * world / (ms / 1e3)
 
 
 def decode_step(S, torch, data, outs, seqlens, cfg, dev, stream, peak, reps=5):
