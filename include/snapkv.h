@@ -169,6 +169,32 @@ int snapkv_compress_ex(const snapkv_shape *shape, const void *q_win, const void 
                        void *stream, int32_t flags);
 
 /*
+ * All-query ("heavy hitter") scoring, a scoring variant: every prompt query
+ * votes instead of the observation window -- the accumulated attention H2O
+ * uses, the method the SnapKV summary compares against (hotpaper.ai summary,
+ * "주요 결과").  For each prefix key j < P_b of KV head h:
+ *
+ *   raw[j] = (1/g) sum_{hq in group} sum_{i=j}^{L_b-1} exp(q_i . k_j / sqrt(d) - lse_all[i, hq])
+ *
+ * then pooling, selection and emission exactly as snapkv_compress.  The
+ * cost is quadratic in the prompt (~L^2/2 * H_q * d multiply-adds), which is
+ * why SnapKV looks only at a window.
+ *   q_all    device, [T, H_q, d] (packed like k), element type shape->dtype,
+ *            16-byte aligned: every prompt query.
+ *   lse_all  device, fp32 [T, H_q], 4-byte aligned: natural-log LSE of each
+ *            query row over the keys it sees (j <= i) with these q and k, as
+ *            the prefill attention computes it; trusted, not checked.
+ * Every other argument, the workspace and the outputs are those of
+ * snapkv_compress (W = the recent window that is always kept).
+ */
+int snapkv_compress_all_queries(const snapkv_shape *shape, const void *q_all, const void *k,
+                                const void *v, const float *lse_all,
+                                const int32_t *seqlens_host, int32_t W, int32_t kernel_size,
+                                int32_t pool_type, int32_t C, void *out_k, void *out_v,
+                                int32_t *out_idx, void *workspace, size_t workspace_bytes,
+                                void *stream);
+
+/*
  * snapkv_compress and snapkv_score with the window rows' log-sum-exp given
  * by the caller.  The prefill attention that precedes SnapKV already
  * normalises every window query row over its causally visible keys (the

@@ -53,6 +53,8 @@ struct Plan {
   float2* stats;     // [total_pieces * Wp] (running max, sum of exp) per piece and row
   float* lse;        // [nseq * H_kv * Wp] natural-log LSE per (sequence, head, row)
   const float* lse_in;  // caller's window LSE [B, W, H_q] (natural log), or null
+  const void* q_all;     // all-query scoring: every prompt query [T, H_q, d], or null
+  const float* lse_all;  // and its rows' natural-log LSE [T, H_q]
   // output heads: H_kv (scores averaged over each KV head's query group), or
   // H_q when every query head selects for itself (head_div = g: output head
   // o gathers KV head o / head_div)
@@ -70,5 +72,6 @@ void count_launches(int n);
 // Launchers (each returns a cudaError_t as int).
 int launch_score_simt(const Plan& p, void* stream);
 int launch_select_gather(const Plan& p, void* stream);
+int launch_score_allq(const Plan& p, void* stream);
 
 }  // namespace snapkv

@@ -163,7 +163,7 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
             const int32_t* seqlens_host, int32_t W, int32_t kernel_size, int32_t pool_type,
             int32_t C, void* out_k, void* out_v, int32_t* out_idx, void* workspace,
             size_t workspace_bytes, void* stream, bool score_only, const float* lse_in,
-            bool per_q = false) {
+            bool per_q = false, const void* q_all = nullptr, const float* lse_all = nullptr) {
   int rc = check_problem(shape, seqlens_host, W, C);
   if (rc == SNAPKV_ERR_INVALID_ARG) return rc;
   if (!q_win || !k || !workspace) return SNAPKV_ERR_INVALID_ARG;
@@ -213,6 +213,8 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
   p.stats = reinterpret_cast<float2*>(ws + lay.stats);
   p.lse = reinterpret_cast<float*>(ws + lay.lse);
   p.lse_in = lse_in;
+  p.q_all = q_all;
+  p.lse_all = lse_all;
   p.out_heads = per_q ? p.H_q : H;
   p.head_div = per_q ? p.g : 1;
   p.status = reinterpret_cast<int*>(ws + lay.status);
@@ -241,7 +243,9 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
       row0 += S.L;
     }
     p.total_pieces = piece;
-    if (piece > 0) {
+    if (piece > 0 && q_all) {
+      if (launch_score_allq(p, stream) != cudaSuccess) return SNAPKV_ERR_CUDA;
+    } else if (piece > 0) {
       bool taken = false;
       if (launch_score_tc(p, stream, &taken) != cudaSuccess) return SNAPKV_ERR_CUDA;
       if (!taken && launch_score_simt(p, stream) != cudaSuccess) return SNAPKV_ERR_CUDA;
@@ -277,6 +281,20 @@ int snapkv_compress_ex(const snapkv_shape* shape, const void* q_win, const void*
   return enqueue(shape, q_win, k, v, seqlens_host, W, kernel_size, pool_type, C, out_k, out_v,
                  out_idx, workspace, workspace_bytes, stream, false, nullptr,
                  (flags & SNAPKV_PER_QUERY_HEAD) != 0);
+}
+
+int snapkv_compress_all_queries(const snapkv_shape* shape, const void* q_all, const void* k,
+                                const void* v, const float* lse_all,
+                                const int32_t* seqlens_host, int32_t W, int32_t kernel_size,
+                                int32_t pool_type, int32_t C, void* out_k, void* out_v,
+                                int32_t* out_idx, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  if (!q_all || !lse_all || !aligned(q_all, 16) || !aligned(lse_all, 4))
+    return SNAPKV_ERR_INVALID_ARG;
+  // q_all stands in for q_win in the argument checks; only q_all is read
+  return enqueue(shape, q_all, k, v, seqlens_host, W, kernel_size, pool_type, C, out_k, out_v,
+                 out_idx, workspace, workspace_bytes, stream, false, nullptr, false, q_all,
+                 lse_all);
 }
 
 int snapkv_compress_with_lse(const snapkv_shape* shape, const void* q_win, const void* k,

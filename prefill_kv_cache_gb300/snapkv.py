@@ -35,6 +35,7 @@ EXPORTED = (
     "snapkv_workspace_size_ex",
     "snapkv_score_offsets_ex",
     "snapkv_compress_ex",
+    "snapkv_compress_all_queries",
     "snapkv_score_offsets",
     "snapkv_get_status",
     "snapkv_host_staging_size",
@@ -96,6 +97,9 @@ def load() -> ctypes.CDLL:
     lib.snapkv_compress_ex.argtypes = [shp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, vp,
                                        sz, vp, i32]
     lib.snapkv_compress_ex.restype = ctypes.c_int
+    lib.snapkv_compress_all_queries.argtypes = [shp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp,
+                                                vp, vp, vp, sz, vp]
+    lib.snapkv_compress_all_queries.restype = ctypes.c_int
     lib.snapkv_kernel_launches.argtypes = []
     lib.snapkv_kernel_launches.restype = ctypes.c_uint64
     lib.snapkv_score_offsets.argtypes = [shp, vp, i32, i32, ctypes.POINTER(sz),
@@ -423,3 +427,32 @@ def selftest_wait(workspace: torch.Tensor, set_flag: bool, stream=None) -> int:
     if rc:
         raise SnapKVError(rc, "snapkv_selftest_wait")
     return get_status(workspace, stream)
+
+
+def compress_all_queries(q_all: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                         lse_all: torch.Tensor, seqlens, window_size: int, kernel_size: int,
+                         pooling, max_capacity_prompt: int, stream=None):
+    """snapkv_compress_all_queries (include/snapkv.h): every prompt query
+    votes.  q_all [T, H_q, d] like k; lse_all fp32 [T, H_q].  Returns
+    (out_k, out_v, out_idx, workspace)."""
+    T, H_q, d = q_all.shape
+    B = len(seqlens)
+    H_kv = k.shape[1]
+    C, W = int(max_capacity_prompt), int(window_size)
+    if lse_all.dtype != torch.float32 or tuple(lse_all.shape) != (T, H_q) or \
+            not lse_all.is_contiguous():
+        raise ValueError(f"lse_all must be a contiguous float32 tensor of shape {(T, H_q)}")
+    shape = make_shape(B, H_q, H_kv, d, q_all.dtype)
+    out_k = torch.empty((B, C, H_kv, d), dtype=k.dtype, device=k.device)
+    out_v = torch.empty((B, C, H_kv, d), dtype=k.dtype, device=k.device)
+    out_idx = torch.empty((B, H_kv, C), dtype=torch.int32, device=k.device)
+    workspace = torch.empty(workspace_size(shape, seqlens, W, C), dtype=torch.uint8,
+                            device=k.device)
+    arr, _ = _seqlens_array(seqlens)
+    rc = load().snapkv_compress_all_queries(
+        ctypes.byref(shape), q_all.data_ptr(), k.data_ptr(), v.data_ptr(), lse_all.data_ptr(),
+        arr, W, int(kernel_size), pool_code(pooling), C, out_k.data_ptr(), out_v.data_ptr(),
+        out_idx.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    if rc:
+        raise SnapKVError(rc, "snapkv_compress_all_queries")
+    return out_k, out_v, out_idx, workspace
