@@ -431,7 +431,8 @@ def decode_step(S, torch, data, outs, seqlens, cfg, dev, stream, peak, reps=5):
 
 
 def run_e2e(S, torch, data, seqlens, cfg, shape, dev, stream, args, layers):
-    """Same metric through snapkv_compress_host: pinned host in, pinned host out."""
+    """Same metric through snapkv_compress_host: pinned host in, pinned host out
+    (V stays on the host; the gather reads the kept rows in place)."""
     W, C, kp, pool = cfg["W"], cfg["C"], cfg["k_pool"], cfg["pool"]
     B = len(seqlens)
     H_kv, d = cfg["H_kv"], cfg["d"]
@@ -462,7 +463,11 @@ def run_e2e(S, torch, data, seqlens, cfg, shape, dev, stream, args, layers):
         step()
     torch.cuda.synchronize()
     sec = (time.perf_counter() - t0) / args.steps
-    h2d = sum(sum(x.numel() * x.element_size() for x in layer) for layer in host)
+    # q_win and K are copied whole; page-locked V is read in place by the
+    # gather, so only the kept rows (C per sequence and KV head) cross the link
+    kept_v = sum(min(int(L), C) for L in seqlens) * H_kv * d * host[0][2].element_size()
+    h2d = sum(q.numel() * q.element_size() + k.numel() * k.element_size() + kept_v
+              for q, k, _ in host)
     d2h = sum(sum(x.numel() * x.element_size() for x in o) for o in outs)
     return {"value": sum(seqlens) * layers / sec, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": 1e3 * sec}

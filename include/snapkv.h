@@ -250,10 +250,13 @@ int snapkv_get_status(const void *workspace, size_t workspace_bytes, void *strea
 /*
  * Host-buffer variant.  Inputs and outputs are host arrays with the layouts
  * of snapkv_compress (page-locked memory makes the copies asynchronous and
- * fast).  The call copies q_win, k and v to `staging` on the device, runs
- * snapkv_compress there, copies out_k, out_v and out_idx back and waits for
- * the stream, so the outputs are complete when it returns.  staging: device,
- * 256-byte aligned, at least snapkv_host_staging_size bytes.
+ * fast).  The call copies q_win and k to `staging` on the device, runs the
+ * compression there, copies out_k, out_v and out_idx back and waits for the
+ * stream, so the outputs are complete when it returns.  Only the kept rows
+ * of v are ever read: page-locked v is read in place by the gather (those
+ * rows cross the host link, the rest never move); pageable v is copied to
+ * staging whole.  staging: device, 256-byte aligned, at least
+ * snapkv_host_staging_size bytes.
  */
 size_t snapkv_host_staging_size(const snapkv_shape *shape, const int32_t *seqlens_host,
                                 int32_t W, int32_t C);

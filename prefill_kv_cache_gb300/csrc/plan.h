@@ -59,6 +59,7 @@ struct Plan {
   // H_q when every query head selects for itself (head_div = g: output head
   // o gathers KV head o / head_div)
   int out_heads, head_div;
+  int v_zero_copy;  // v is page-locked host memory read in place (plain loads only)
   int* status;       // device status word
   int* counters;     // work-queue head and per-group completion counters
   long long total_rows;  // rows of k / v in the whole call (T)

@@ -513,7 +513,8 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
   cluster.sync();
   const int share = (p.C + CS - 1) / CS;
   const int s0 = min(p.C, rank * share), s1 = min(p.C, s0 + share);
-  const bool bulk = cap_floats * 4 >= 2 * row_bytes;
+  // bulk copies read device memory only; host-resident V goes through plain loads
+  const bool bulk = !p.v_zero_copy && cap_floats * 4 >= 2 * row_bytes;
   for (int c0 = s0; c0 < s1; c0 += kChunk) {
     const int m = min(kChunk, s1 - c0);
     __syncthreads();  // sel_pos free

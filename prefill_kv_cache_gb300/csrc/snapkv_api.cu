@@ -163,7 +163,8 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
             const int32_t* seqlens_host, int32_t W, int32_t kernel_size, int32_t pool_type,
             int32_t C, void* out_k, void* out_v, int32_t* out_idx, void* workspace,
             size_t workspace_bytes, void* stream, bool score_only, const float* lse_in,
-            bool per_q = false, const void* q_all = nullptr, const float* lse_all = nullptr) {
+            bool per_q = false, const void* q_all = nullptr, const float* lse_all = nullptr,
+            bool v_zero_copy = false) {
   int rc = check_problem(shape, seqlens_host, W, C);
   if (rc == SNAPKV_ERR_INVALID_ARG) return rc;
   if (!q_win || !k || !workspace) return SNAPKV_ERR_INVALID_ARG;
@@ -215,6 +216,7 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
   p.lse_in = lse_in;
   p.q_all = q_all;
   p.lse_all = lse_all;
+  p.v_zero_copy = v_zero_copy ? 1 : 0;
   p.out_heads = per_q ? p.H_q : H;
   p.head_div = per_q ? p.g : 1;
   p.status = reinterpret_cast<int*>(ws + lay.status);
@@ -377,13 +379,27 @@ int snapkv_compress_host(const snapkv_shape* shape, const void* q_win_host, cons
   if (staging_bytes < h.total) return SNAPKV_ERR_WORKSPACE;
   char* base = static_cast<char*>(staging);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Only the kept V rows are ever read: page-locked V stays on the host and
+  // the gather reads those rows in place, instead of uploading all of V.
+  const void* v_dev = base + h.v;
+  bool v_zero_copy = false;
+  {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, v_host) == cudaSuccess && at.type == cudaMemoryTypeHost &&
+        at.devicePointer != nullptr && aligned(at.devicePointer, 16)) {
+      v_dev = at.devicePointer;
+      v_zero_copy = true;
+    }
+    cudaGetLastError();  // a pageable pointer is not an error here
+  }
   if (cudaMemcpyAsync(base + h.q, q_win_host, h.q_bytes, cudaMemcpyHostToDevice, st) ||
       cudaMemcpyAsync(base + h.k, k_host, h.kv_bytes, cudaMemcpyHostToDevice, st) ||
-      cudaMemcpyAsync(base + h.v, v_host, h.kv_bytes, cudaMemcpyHostToDevice, st))
+      (!v_zero_copy &&
+       cudaMemcpyAsync(base + h.v, v_host, h.kv_bytes, cudaMemcpyHostToDevice, st)))
     return SNAPKV_ERR_CUDA;
-  rc = snapkv_compress(shape, base + h.q, base + h.k, base + h.v, seqlens_host, W, kernel_size,
-                       pool_type, C, base + h.ok, base + h.ov,
-                       reinterpret_cast<int32_t*>(base + h.oi), base + h.ws, h.ws_bytes, stream);
+  rc = enqueue(shape, base + h.q, base + h.k, v_dev, seqlens_host, W, kernel_size, pool_type, C,
+               base + h.ok, base + h.ov, reinterpret_cast<int32_t*>(base + h.oi), base + h.ws,
+               h.ws_bytes, stream, false, nullptr, false, nullptr, nullptr, v_zero_copy);
   if (rc != SNAPKV_OK) return rc;
   if (cudaMemcpyAsync(out_k_host, base + h.ok, h.out_bytes, cudaMemcpyDeviceToHost, st) ||
       cudaMemcpyAsync(out_v_host, base + h.ov, h.out_bytes, cudaMemcpyDeviceToHost, st) ||

@@ -104,12 +104,17 @@ def test_repeated_calls_reuse_workspace():
         assert torch.equal(x, y)
 
 
-def test_host_buffer_entry_point_matches_device():
+@pytest.mark.parametrize("pinned_v", [True, False])
+def test_host_buffer_entry_point_matches_device(pinned_v):
+    """Page-locked V is read in place by the gather (only the kept rows cross
+    the link); pageable V is uploaded whole.  Both match the device call."""
     lay = synth.make_inputs(10, [4000, 700], 32, 8, 128, 32, "bf16", nspans=4)
     C = 1024
     gpu = parity.run_gpu(lay, 7, "avg", C)
     q, k, v = (torch.from_numpy(x).view(torch.bfloat16).pin_memory()
                for x in (lay.q_win, lay.k, lay.v))
+    if not pinned_v:
+        v = torch.from_numpy(lay.v.copy()).view(torch.bfloat16)
     B, H_kv, d = lay.B, lay.H_kv, lay.d
     ok = torch.empty((B, C, H_kv, d), dtype=torch.bfloat16).pin_memory()
     ov = torch.empty_like(ok)
