@@ -3,9 +3,10 @@
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg use this package.  The CUDA library never imports,
 links or runs it, and it shares no code with the CUDA library.  The arithmetic
-lives in ``snapkv_ref.c`` (plain C, fp64; compression) and ``decode.py``
-(numpy, fp64; one decode step of attention over a cache) and ``allq.py``
-(numpy, fp64; all-query scoring); this module only
+lives in ``snapkv_ref.c`` (plain C, fp64; compression), ``decode.py``
+(numpy, fp64; one decode step of attention over a cache), ``allq.py``
+(numpy, fp64; all-query scoring) and ``scissorhands.py`` (numpy, fp64;
+Scissorhands decode-time eviction); this module only
 marshals numpy arrays and builds the shared object with gcc.
 """
 from __future__ import annotations
@@ -18,6 +19,7 @@ import numpy as np
 
 from .decode import decode_attention  # noqa: F401
 from .allq import compress_all_queries, scores_all_queries  # noqa: F401
+from . import scissorhands  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "snapkv_ref.c")
