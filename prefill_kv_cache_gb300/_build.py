@@ -35,7 +35,8 @@ def sources() -> list[str]:
 
 
 def _deps() -> list[str]:
-    return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "snapkv.h")]
+    return ([os.path.join(CSRC, f) for f in os.listdir(CSRC)] +
+            [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)])
 
 
 def up_to_date() -> bool:

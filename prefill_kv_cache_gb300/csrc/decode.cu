@@ -23,6 +23,12 @@
 //                  the V rows (coalesced).  The CTA merges its warps and
 //                  writes (max, sum, unnormalised output) per query head.
 //   decode_combine grid (B, H_q): merges the chunks of each sequence.
+//
+// The Scissorhands instantiation (SH = true) serves one step of the
+// decode-time eviction in scissorhands.cu: the rows of each sequence come from
+// the device-side cache state (the step's append and eviction already ran),
+// every logit is also stored for the history marks, and the combine stores
+// each query head's final (max, sum).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -32,6 +38,7 @@
 #include <cstring>
 
 #include "plan.h"
+#include "sh_attention.h"
 #include "snapkv.h"
 
 namespace snapkv {
@@ -60,6 +67,11 @@ struct Params {
   float* part_o;    // [total_chunks, H_kv, g, d]
   float2* part_ml;  // [total_chunks, H_kv, g]: (max of log2-scaled logits, sum of exp2)
   int b0;           // batch index of seq[0]
+  // Scissorhands step only
+  const int* sh_state;  // [B, 4]: rows before the step's append, ...
+  int sh_budget, sh_evict, sh_cap;
+  float* sh_logits;     // [B, H_kv, cap, g]: log2-scaled logits
+  float2* sh_ml;        // [B, H_q]: final (max, sum of exp2)
   Seq seq[kGroup];
 };
 
@@ -129,7 +141,7 @@ __device__ __forceinline__ void load_cols<float, 2>(const float* p, float* f) {
   f[0] = a.x; f[1] = a.y;
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool SH>
 __global__ void __launch_bounds__(kThreads) decode_chunk(const __grid_constant__ Params p) {
   constexpr int DL = D / 32;
   extern __shared__ __align__(16) float sm[];
@@ -149,7 +161,13 @@ __global__ void __launch_bounds__(kThreads) decode_chunk(const __grid_constant__
   const Seq& S = p.seq[lo];
   const int b = p.b0 + lo;
   const int j0 = (ch - S.chunk0) * p.chunk;
-  const int j1 = min(S.n, j0 + p.chunk);
+  int rows = S.n;
+  if constexpr (SH) {  // the rows after this step's append and eviction
+    rows = p.sh_state[b * 4] + 1;
+    if (rows > p.sh_budget) rows -= p.sh_evict;
+    rows = min(max(rows, 0), p.sh_cap);
+  }
+  const int j1 = min(rows, j0 + p.chunk);
   __syncthreads();  // the previous unit's shared-memory readers are done
 
   const T* qb = static_cast<const T*>(p.q) + ((size_t)b * p.H_q + (size_t)h * G) * D;
@@ -202,6 +220,19 @@ __global__ void __launch_bounds__(kThreads) decode_chunk(const __grid_constant__
           s[x] = fmaf(qc.y, kf[5], s[x]);
           s[x] = fmaf(qc.z, kf[6], s[x]);
           s[x] = fmaf(qc.w, kf[7], s[x]);
+        }
+      }
+    }
+    if constexpr (SH) {
+      if (live) {
+        float* lg = p.sh_logits + (((size_t)b * p.H_kv + h) * p.sh_cap + j) * G;
+        if constexpr (G % 4 == 0) {
+#pragma unroll
+          for (int x = 0; x < G; x += 4)
+            *reinterpret_cast<float4*>(lg + x) = make_float4(s[x], s[x + 1], s[x + 2], s[x + 3]);
+        } else {
+#pragma unroll
+          for (int x = 0; x < G; ++x) lg[x] = s[x];
         }
       }
     }
@@ -272,6 +303,7 @@ __global__ void __launch_bounds__(kThreads) decode_chunk(const __grid_constant__
 }
 
 // Grid (nseq, H_q), D threads: merges the chunks of one sequence and head.
+template <bool SH>
 __global__ void decode_combine(const __grid_constant__ Params p) {
   const int s = blockIdx.x, hq = blockIdx.y, c = threadIdx.x;
   const Seq& S = p.seq[s];
@@ -290,6 +322,9 @@ __global__ void decode_combine(const __grid_constant__ Params p) {
     O += p.part_o[(unit * p.g + x) * p.d + c] * f;
   }
   p.out[((size_t)(p.b0 + s) * p.H_q + hq) * p.d + c] = O / L;
+  if constexpr (SH) {
+    if (c == 0) p.sh_ml[(size_t)(p.b0 + s) * p.H_q + hq] = make_float2(M, L);
+  }
 }
 
 int sm_count() {
@@ -303,7 +338,7 @@ int sm_count() {
   return sms;
 }
 
-template <typename T, int D>
+template <typename T, int D, bool SH = false>
 cudaError_t launch_typed(const Params& p, cudaStream_t st) {
   const size_t smem = ((size_t)p.g * D + kWarps * p.g * 2 + (size_t)kWarps * p.g * D) * sizeof(float);
   const int units = p.total_chunks * p.H_kv;
@@ -321,15 +356,15 @@ cudaError_t launch_typed(const Params& p, cudaStream_t st) {
     }
   };
   switch (p.g) {
-    case 1: go(decode_chunk<T, D, 1>); break;
-    case 2: go(decode_chunk<T, D, 2>); break;
-    case 4: go(decode_chunk<T, D, 4>); break;
-    case 8: go(decode_chunk<T, D, 8>); break;
-    case 16: go(decode_chunk<T, D, 16>); break;
+    case 1: go(decode_chunk<T, D, 1, SH>); break;
+    case 2: go(decode_chunk<T, D, 2, SH>); break;
+    case 4: go(decode_chunk<T, D, 4, SH>); break;
+    case 8: go(decode_chunk<T, D, 8, SH>); break;
+    case 16: go(decode_chunk<T, D, 16, SH>); break;
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  decode_combine<<<dim3(p.nseq, p.H_q), D, 0, st>>>(p);
+  decode_combine<SH><<<dim3(p.nseq, p.H_q), D, 0, st>>>(p);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launches(2);
   return e;
@@ -377,6 +412,60 @@ size_t max_units(const snapkv_shape* sh, const int32_t* lens) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace dec
+
+size_t sh_attention_units(int B, int cap, int H_kv) {
+  const size_t per = (size_t)(cap + dec::kMinChunk - 1) / dec::kMinChunk;
+  return (size_t)std::min(B, dec::kGroup) * per * H_kv;
+}
+
+int launch_sh_attention(const ShAttention& a, void* stream) {
+  dec::Params* pp = new dec::Params;
+  dec::Params& p = *pp;
+  std::memset(&p, 0, sizeof p);
+  p.H_q = a.H_q;
+  p.H_kv = a.H_kv;
+  p.g = a.H_q / a.H_kv;
+  p.d = a.d;
+  p.dtype = a.dtype;
+  p.c2 = (float)(1.4426950408889634 / std::sqrt((double)a.d));
+  p.q = a.q;
+  p.k = a.k;
+  p.v = a.v;
+  p.out = a.out;
+  p.part_o = a.part_o;
+  p.part_ml = a.part_ml;
+  p.sh_state = a.state;
+  p.sh_budget = a.budget;
+  p.sh_evict = a.evict;
+  p.sh_cap = a.cap;
+  p.sh_logits = a.logits;
+  p.sh_ml = a.ml;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int sms = dec::sm_count();
+  cudaError_t e = cudaSuccess;
+  for (int g0 = 0; g0 < a.B && e == cudaSuccess; g0 += dec::kGroup) {
+    const int g1 = std::min(a.B, g0 + dec::kGroup);
+    p.nseq = g1 - g0;
+    p.b0 = g0;
+    // chunks sized for the full cache: the rows in use are only known on the device
+    p.chunk = dec::chunk_for((long long)p.nseq * a.cap, a.H_kv, sms);
+    const int per = (a.cap + p.chunk - 1) / p.chunk;
+    for (int s = 0; s < p.nseq; ++s) {
+      p.seq[s].row0 = (long long)(g0 + s) * a.cap;
+      p.seq[s].n = a.cap;
+      p.seq[s].chunk0 = s * per;
+    }
+    p.total_chunks = p.nseq * per;
+    if (p.dtype == SNAPKV_BF16)
+      e = a.d == 64 ? dec::launch_typed<__nv_bfloat16, 64, true>(p, st)
+                    : dec::launch_typed<__nv_bfloat16, 128, true>(p, st);
+    else
+      e = a.d == 64 ? dec::launch_typed<float, 64, true>(p, st)
+                    : dec::launch_typed<float, 128, true>(p, st);
+  }
+  delete pp;
+  return e;
+}
 }  // namespace snapkv
 
 using namespace snapkv;
