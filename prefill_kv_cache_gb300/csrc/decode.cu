@@ -12,16 +12,25 @@
 //
 // over the sequence's n_b cached rows.  The step reads every cached K and V
 // byte once and does ~2 multiply-adds per byte: it is HBM-bound, so it runs
-// on the CUDA cores (split-K "flash decoding"):
+// on the CUDA cores (split-K "flash decoding"), with the cache streamed
+// through shared memory by the bulk-copy (TMA) engine:
 //
-//   decode_chunk   grid (key chunks of all sequences, H_kv), 8 warps.  A
-//                  warp takes blocks of 32 keys: each lane computes its key's
-//                  logits for the g query heads of the group from a whole K
-//                  row (16-byte loads), the warp updates the running max and
-//                  sum of exp2, then walks the block's keys broadcasting their
-//                  weights while each lane accumulates its d/32 columns of
-//                  the V rows (coalesced).  The CTA merges its warps and
-//                  writes (max, sum, unnormalised output) per query head.
+//   decode_chunk   persistent, one CTA per SM; work units are (key chunk,
+//                  KV head).  Each warp owns a contiguous share of a unit's
+//                  rows and streams it in blocks of 32 rows through its own
+//                  ring of shared-memory stages: one lane issues the TMA
+//                  tensor copies of the block's K and V (boxes of 32 rows x
+//                  128 bytes, 128-byte swizzle), which complete on the
+//                  stage's mbarrier, and the next stages are in flight while
+//                  the current one is computed -- blocks of the next unit
+//                  included.  The swizzle puts the 16-byte pieces of 8
+//                  consecutive rows in distinct banks, so the per-lane row
+//                  reads of the logit phase are conflict-free.  Lane i
+//                  computes row i's logits for the
+//                  g query heads of the group; the warp updates its running
+//                  max and sum of exp2; each lane then accumulates its d/32
+//                  columns over the block's V rows.  The CTA merges its warps
+//                  and writes (max, sum, unnormalised output) per query head.
 //   decode_combine grid (B, H_q): merges the chunks of each sequence.
 //
 // The Scissorhands instantiation (SH = true) serves one step of the
@@ -29,8 +38,10 @@
 // the device-side cache state (the step's append and eviction already ran),
 // every logit is also stored for the history marks, and the combine stores
 // each query head's final (max, sum).
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cmath>
@@ -44,12 +55,13 @@
 namespace snapkv {
 namespace dec {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
 constexpr int kGroup = 512;        // sequences per launch (kernel-parameter table)
-constexpr int kMinChunk = 128;     // keys per CTA, bounds
-constexpr int kMaxChunk = 2048;
-constexpr int kVUnroll = 8;        // V rows loaded ahead of their multiply-adds
+constexpr int kMinChunk = 128;     // keys per unit, bounds
+constexpr int kMaxChunk = 16384;
+constexpr int kRows = 32;          // rows per block: one per lane
+constexpr int kMaxWarps = 8;
+constexpr uint64_t kWaitNs = 2000000000ull;  // a stage that has not landed in 2 s
+constexpr int kBoxBytes = kRows * 128;       // one TMA box: 32 rows x 128 bytes
 
 struct Seq {
   long long row0;  // first cache row of the sequence (a row = H_kv * d elements)
@@ -59,6 +71,7 @@ struct Seq {
 
 struct Params {
   int nseq, H_q, H_kv, g, d, dtype, chunk, total_chunks;
+  int warps, stages, nbw;  // warps per CTA, stages per warp, blocks per warp per unit
   float c2;  // log2(e) / sqrt(d)
   const void* q;
   const void* k;
@@ -67,6 +80,7 @@ struct Params {
   float* part_o;    // [total_chunks, H_kv, g, d]
   float2* part_ml;  // [total_chunks, H_kv, g]: (max of log2-scaled logits, sum of exp2)
   int b0;           // batch index of seq[0]
+  long long rows_total;  // rows of the k / v arrays (the tensor maps' extent)
   // Scissorhands step only
   const int* sh_state;  // [B, 4]: rows before the step's append, ...
   int sh_budget, sh_evict, sh_cap;
@@ -92,12 +106,47 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-// 8 consecutive elements of a row as fp32
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ bool bar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred q;\n mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n"
+      " selp.b32 %0, 1, 0, q;\n}\n"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait for a stage; false once the CTA is aborting (its flag was
+// already up, or this wait ran out and raised it).
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (bar_test(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (bar_test(bar, parity)) return true;
+    if ((it & 31) == 0) {
+      if (*abort) return false;
+      if (global_ns() - t0 > kWaitNs) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// 8 consecutive elements of a row in shared memory as fp32
 template <typename T>
-__device__ __forceinline__ void load8(const T* p, float* f);
+__device__ __forceinline__ void lds8(const unsigned char* p, float* f);
 template <>
-__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float* f) {
-  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+__device__ __forceinline__ void lds8<__nv_bfloat16>(const unsigned char* p, float* f) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -105,200 +154,340 @@ __device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, flo
     f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
   }
 }
-template <>
-__device__ __forceinline__ void load8<float>(const float* p, float* f) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-}
 
-// this lane's DL = D / 32 consecutive columns of a V row as fp32
+// DL consecutive elements of a row in shared memory as fp32
 template <typename T, int DL>
-__device__ __forceinline__ void load_cols(const T* p, float* f);
-template <>
-__device__ __forceinline__ void load_cols<__nv_bfloat16, 4>(const __nv_bfloat16* p, float* f) {
-  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
-  f[0] = __uint_as_float(u.x << 16);
-  f[1] = __uint_as_float(u.x & 0xffff0000u);
-  f[2] = __uint_as_float(u.y << 16);
-  f[3] = __uint_as_float(u.y & 0xffff0000u);
-}
-template <>
-__device__ __forceinline__ void load_cols<__nv_bfloat16, 2>(const __nv_bfloat16* p, float* f) {
-  const uint32_t u = __ldg(reinterpret_cast<const unsigned int*>(p));
-  f[0] = __uint_as_float(u << 16);
-  f[1] = __uint_as_float(u & 0xffff0000u);
-}
-template <>
-__device__ __forceinline__ void load_cols<float, 4>(const float* p, float* f) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-}
-template <>
-__device__ __forceinline__ void load_cols<float, 2>(const float* p, float* f) {
-  const float2 a = __ldg(reinterpret_cast<const float2*>(p));
-  f[0] = a.x; f[1] = a.y;
+__device__ __forceinline__ void lds_cols(const unsigned char* p, float* f) {
+  if constexpr (sizeof(T) == 2 && DL == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    f[0] = __uint_as_float(u.x << 16);
+    f[1] = __uint_as_float(u.x & 0xffff0000u);
+    f[2] = __uint_as_float(u.y << 16);
+    f[3] = __uint_as_float(u.y & 0xffff0000u);
+  } else if constexpr (sizeof(T) == 2 && DL == 2) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    f[0] = __uint_as_float(u << 16);
+    f[1] = __uint_as_float(u & 0xffff0000u);
+  } else if constexpr (DL == 4) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  } else {
+    const float2 a = *reinterpret_cast<const float2*>(p);
+    f[0] = a.x; f[1] = a.y;
+  }
 }
 
-template <typename T, int D, int G, bool SH>
-__global__ void __launch_bounds__(kThreads) decode_chunk(const __grid_constant__ Params p) {
-  constexpr int DL = D / 32;
-  extern __shared__ __align__(16) float sm[];
-  float* qs = sm;                        // [G][D], pre-scaled by log2(e)/sqrt(d)
-  float* wml = qs + G * D;               // [kWarps][G][2]
-  float* wacc = wml + kWarps * G * 2;    // [kWarps][G][D]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // persistent: units (chunk, KV head), the heads of a chunk side by side
-  for (int unit_i = blockIdx.x; unit_i < p.total_chunks * p.H_kv; unit_i += gridDim.x) {
-  const int ch = unit_i / p.H_kv, h = unit_i % p.H_kv;
-  // the sequence of this chunk
+// Shared-memory bytes of one slot: 32 K (or V) rows as 128-byte wide boxes
+// (a row of D * esize bytes spans D * esize / 128 boxes).
+__host__ __device__ constexpr int boxes(int D, int esize) { return D * esize / 128; }
+__host__ __device__ constexpr int slot_bytes(int D, int esize) {
+  return boxes(D, esize) * kBoxBytes;
+}
+// Byte address of byte o of row r within a 128-byte-swizzled K or V block:
+// 16-byte piece c of row r sits at piece c ^ (r mod 8) of its 128-byte line.
+__device__ __forceinline__ int swz(int r, int o) {
+  return (o >> 7) * kBoxBytes + r * 128 + ((((o >> 4) & 7) ^ (r & 7)) << 4) + (o & 15);
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+// Where the unit's rows of one sequence start and end.
+struct UnitRows {
+  int seq, h, j0, j1;
+};
+
+template <bool SH>
+__device__ __forceinline__ UnitRows unit_rows(const Params& p, int unit_i) {
+  const int ch = unit_i / p.H_kv;
+  UnitRows u;
+  u.h = unit_i % p.H_kv;
   int lo = 0, hi = p.nseq - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (p.seq[mid].chunk0 <= ch) lo = mid; else hi = mid - 1;
   }
+  u.seq = lo;
   const Seq& S = p.seq[lo];
-  const int b = p.b0 + lo;
-  const int j0 = (ch - S.chunk0) * p.chunk;
   int rows = S.n;
   if constexpr (SH) {  // the rows after this step's append and eviction
-    rows = p.sh_state[b * 4] + 1;
+    rows = p.sh_state[(p.b0 + lo) * 4] + 1;
     if (rows > p.sh_budget) rows -= p.sh_evict;
     rows = min(max(rows, 0), p.sh_cap);
   }
-  const int j1 = min(rows, j0 + p.chunk);
-  __syncthreads();  // the previous unit's shared-memory readers are done
+  u.j0 = (ch - S.chunk0) * p.chunk;
+  u.j1 = min(rows, u.j0 + p.chunk);
+  return u;
+}
 
-  const T* qb = static_cast<const T*>(p.q) + ((size_t)b * p.H_q + (size_t)h * G) * D;
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    float f;
-    if constexpr (sizeof(T) == 2)
-      f = __bfloat162float(qb[i]);
-    else
-      f = qb[i];
-    qs[i] = f * p.c2;
-  }
+template <typename T, int D, int G, bool SH>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1)
+    decode_chunk(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v) {
+  constexpr int DL = D / 32;
+  constexpr int NB = boxes(D, (int)sizeof(T));
+  constexpr int SLOT = slot_bytes(D, (int)sizeof(T));
+  constexpr int EPB = 128 / (int)sizeof(T);  // elements per box row
+  extern __shared__ __align__(1024) unsigned char sm_raw[];
+  // the swizzle pattern repeats every 1024 bytes: boxes start on such a boundary
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // per warp: NS K slots and one V slot (the next block's V is fetched while
+  // its logits are computed)
+  const int warps = p.warps, NS = p.stages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* kslots = sm + (size_t)warp * (NS + 1) * SLOT;
+  unsigned char* vslot = kslots + (size_t)NS * SLOT;
+  uint64_t* bars0 = reinterpret_cast<uint64_t*>(sm + (size_t)warps * (NS + 1) * SLOT);
+  uint64_t* kbars = bars0 + warp * (NS + 1);
+  uint64_t* vbar = kbars + NS;
+  float* qs = reinterpret_cast<float*>(bars0 + warps * (NS + 1));  // [G][D], pre-scaled
+  float* pwb = qs + G * D + warp * kRows * G;        // this warp's [32][G] weights
+  float* wml = qs + G * D + warps * kRows * G;       // [warps][G][2]
+  float* wacc = wml + warps * G * 2;                 // [warps][G][D]
+  volatile int* abort = reinterpret_cast<volatile int*>(wacc + warps * G * D);
+
+  const int nunits = p.total_chunks * p.H_kv;
+  const int my_units =
+      (int)blockIdx.x < nunits ? (nunits - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  const int total = my_units * p.nbw;  // blocks in this warp's stream
+  if (threadIdx.x == 0) *abort = 0;
+  if (lane == 0)
+    for (int s = 0; s <= NS; ++s)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&kbars[s])) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
 
-  const size_t row_elems = (size_t)p.H_kv * D;
-  const T* kbase = static_cast<const T*>(p.k) + (size_t)S.row0 * row_elems + (size_t)h * D;
-  const T* vbase = static_cast<const T*>(p.v) + (size_t)S.row0 * row_elems + (size_t)h * D;
+  // the rows [first, first + count) of block n of this warp's stream
+  auto block_rows = [&](int n, int& seq, int& h, int& first, int& count) {
+    const int k = n / p.nbw, m = n % p.nbw;
+    const UnitRows u = unit_rows<SH>(p, (int)blockIdx.x + k * (int)gridDim.x);
+    seq = u.seq;
+    h = u.h;
+    first = u.j0 + (warp * p.nbw + m) * kRows;
+    count = min(kRows, u.j1 - first);
+    if (count < 0) count = 0;
+  };
+  // lane 0 copies block n's K (or V) boxes into a slot (rows past the end of
+  // the cache arrive as zeros and are not used)
+  int k_issued = 0, k_landed = 0, v_issued = 0, v_landed = 0;  // blocks, in order
+  auto issue = [&](int n, bool is_v) {
+    const int stop = __shfl_sync(0xffffffffu, *abort, 0);  // one decision for the warp
+    if (n >= total || stop) return;
+    (is_v ? v_issued : k_issued) = n + 1;
+    if (lane != 0) return;
+    int seq, h, first, count;
+    block_rows(n, seq, h, first, count);
+    const uint32_t bar = saddr(is_v ? vbar : &kbars[n % NS]);
+    if (count > 0) {
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                   "r"(SLOT)
+                   : "memory");
+      const uint32_t dst = saddr(is_v ? vslot : kslots + (size_t)(n % NS) * SLOT);
+      const int row = (int)(p.seq[seq].row0 + first);
+#pragma unroll
+      for (int bx = 0; bx < NB; ++bx)
+        tma_load_3d(dst + bx * kBoxBytes, is_v ? &tm_v : &tm_k, bar, bx * EPB, h, row);
+    } else {
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+    }
+  };
 
-  float m[G], l[G], acc[G][DL];
+  // Swizzled offsets depend on a row only through row mod 8: this lane's
+  // K row (logit phase) and its V columns in rows 8i + u (output phase).
+  int koff[8], voff[8];
+  {
+    const int vo = lane * DL * (int)sizeof(T);
 #pragma unroll
-  for (int x = 0; x < G; ++x) {
-    m[x] = -INFINITY;
-    l[x] = 0.f;
-#pragma unroll
-    for (int c = 0; c < DL; ++c) acc[x][c] = 0.f;
+    for (int u = 0; u < 8; ++u) {
+      koff[u] = lane * 128 + ((u ^ (lane & 7)) << 4);
+      voff[u] = (vo >> 7) * kBoxBytes + u * 128 + ((((vo >> 4) & 7) ^ u) << 4) + (vo & 15);
+    }
   }
-  // this warp's keys: a contiguous share of the chunk, in blocks of 32
-  const int per = (p.chunk + kWarps - 1) / kWarps;
-  const int wj0 = j0 + warp * per, wj1 = min(j1, wj0 + per);
-  for (int base = wj0; base < wj1; base += 32) {
-    const int j = base + lane;
-    const bool live = j < wj1;
-    float s[G];
-#pragma unroll
-    for (int x = 0; x < G; ++x) s[x] = 0.f;
-    if (live) {
-      const T* kr = kbase + (size_t)j * row_elems;
-#pragma unroll
-      for (int c = 0; c < D; c += 8) {  // all of the row's loads in flight at once
-        float kf[8];
-        load8<T>(kr + c, kf);
-#pragma unroll
-        for (int x = 0; x < G; ++x) {
-          const float4 qa = *reinterpret_cast<const float4*>(qs + x * D + c);
-          const float4 qc = *reinterpret_cast<const float4*>(qs + x * D + c + 4);
-          s[x] = fmaf(qa.x, kf[0], s[x]);
-          s[x] = fmaf(qa.y, kf[1], s[x]);
-          s[x] = fmaf(qa.z, kf[2], s[x]);
-          s[x] = fmaf(qa.w, kf[3], s[x]);
-          s[x] = fmaf(qc.x, kf[4], s[x]);
-          s[x] = fmaf(qc.y, kf[5], s[x]);
-          s[x] = fmaf(qc.z, kf[6], s[x]);
-          s[x] = fmaf(qc.w, kf[7], s[x]);
-        }
-      }
+
+  for (int n = 0; n < NS; ++n) issue(n, false);
+  issue(0, true);
+  int n = 0;
+  for (int k = 0; k < my_units; ++k) {
+    const int unit_i = (int)blockIdx.x + k * (int)gridDim.x;
+    const UnitRows u = unit_rows<SH>(p, unit_i);
+    const int b = p.b0 + u.seq, h = u.h;
+    __syncthreads();  // the previous unit's merge has read wml / wacc
+    const T* qb = static_cast<const T*>(p.q) + ((size_t)b * p.H_q + (size_t)h * G) * D;
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+      float f;
+      if constexpr (sizeof(T) == 2)
+        f = __bfloat162float(qb[i]);
+      else
+        f = qb[i];
+      qs[i] = f * p.c2;
     }
-    if constexpr (SH) {
-      if (live) {
-        float* lg = p.sh_logits + (((size_t)b * p.H_kv + h) * p.sh_cap + j) * G;
-        if constexpr (G % 4 == 0) {
-#pragma unroll
-          for (int x = 0; x < G; x += 4)
-            *reinterpret_cast<float4*>(lg + x) = make_float4(s[x], s[x + 1], s[x + 2], s[x + 3]);
-        } else {
-#pragma unroll
-          for (int x = 0; x < G; ++x) lg[x] = s[x];
-        }
-      }
-    }
-    float pw[G];
+    __syncthreads();
+
+    // packed fp32 pairs (fma.rn.f32x2): this lane's columns 2i, 2i + 1
+    float m[G], l[G];
+    float2 acc[G][DL / 2];
 #pragma unroll
     for (int x = 0; x < G; ++x) {
-      const float bm = warp_max(live ? s[x] : -INFINITY);
-      const float mn = fmaxf(m[x], bm);
-      pw[x] = live ? ex2(s[x] - mn) : 0.f;
-      const float sc = ex2(m[x] - mn);  // 0 on the first block (m = -inf)
-      l[x] = l[x] * sc + warp_sum(pw[x]);
+      m[x] = -INFINITY;
+      l[x] = 0.f;
 #pragma unroll
-      for (int c = 0; c < DL; ++c) acc[x][c] *= sc;
-      m[x] = mn;
+      for (int c = 0; c < DL / 2; ++c) acc[x][c] = make_float2(0.f, 0.f);
     }
-    const int nk = min(32, wj1 - base);
-    for (int j8 = 0; j8 < nk; j8 += kVUnroll) {
-      float vf[kVUnroll][DL];  // kVUnroll rows' loads in flight
+    for (int mb = 0; mb < p.nbw; ++mb, ++n) {
+      const int s = n % NS;
+      const int first = u.j0 + (warp * p.nbw + mb) * kRows;
+      const int count = max(0, min(kRows, u.j1 - first));
+      // every lane polls; the block is used only if all of them saw it land
+      const bool ready =
+          __all_sync(0xffffffffu, bar_wait(saddr(&kbars[s]), (uint32_t)(n / NS) & 1u, abort));
+      if (ready) k_landed = n + 1;
+      const unsigned char* kst = kslots + (size_t)s * SLOT;
+      const unsigned char* vst = vslot;
+      if (ready && count > 0) {
+        const bool live = lane < count;
+        float sc[G];
 #pragma unroll
-      for (int u = 0; u < kVUnroll; ++u) {
-        const int jj = min(j8 + u, nk - 1);  // past the block end: a row already loaded, weight 0
-        load_cols<T, DL>(vbase + (size_t)(base + jj) * row_elems + lane * DL, vf[u]);
-      }
+        for (int x = 0; x < G; ++x) sc[x] = 0.f;
+        if (live) {
+          // two packed partial sums per query head: four independent pairs
+          float2 pa[G], pb[G];
 #pragma unroll
-      for (int u = 0; u < kVUnroll; ++u) {
+          for (int x = 0; x < G; ++x) {
+            pa[x] = make_float2(0.f, 0.f);
+            pb[x] = make_float2(0.f, 0.f);
+          }
+#pragma unroll
+          for (int c = 0; c < D; c += 8) {
+            float kf[8];
+            if constexpr (sizeof(T) == 2) {  // piece c / 8 of the row
+              lds8<T>(kst + (c >> 6) * kBoxBytes + koff[(c >> 3) & 7], kf);
+            } else {  // 8 floats span pieces c / 4 and c / 4 + 1
+              const float4 a =
+                  *reinterpret_cast<const float4*>(kst + (c >> 5) * kBoxBytes + koff[(c >> 2) & 7]);
+              const float4 b2 = *reinterpret_cast<const float4*>(
+                  kst + ((c + 4) >> 5) * kBoxBytes + koff[((c + 4) >> 2) & 7]);
+              kf[0] = a.x; kf[1] = a.y; kf[2] = a.z; kf[3] = a.w;
+              kf[4] = b2.x; kf[5] = b2.y; kf[6] = b2.z; kf[7] = b2.w;
+            }
+#pragma unroll
+            for (int x = 0; x < G; ++x) {
+              const float4 qa = *reinterpret_cast<const float4*>(qs + x * D + c);
+              const float4 qc = *reinterpret_cast<const float4*>(qs + x * D + c + 4);
+              pa[x] = __ffma2_rn(make_float2(qa.x, qa.y), make_float2(kf[0], kf[1]), pa[x]);
+              pb[x] = __ffma2_rn(make_float2(qa.z, qa.w), make_float2(kf[2], kf[3]), pb[x]);
+              pa[x] = __ffma2_rn(make_float2(qc.x, qc.y), make_float2(kf[4], kf[5]), pa[x]);
+              pb[x] = __ffma2_rn(make_float2(qc.z, qc.w), make_float2(kf[6], kf[7]), pb[x]);
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < G; ++x) sc[x] = (pa[x].x + pa[x].y) + (pb[x].x + pb[x].y);
+          if constexpr (SH) {
+            float* lg = p.sh_logits + (((size_t)b * p.H_kv + h) * p.sh_cap + first + lane) * G;
+            if constexpr (G % 4 == 0) {
+#pragma unroll
+              for (int x = 0; x < G; x += 4)
+                *reinterpret_cast<float4*>(lg + x) =
+                    make_float4(sc[x], sc[x + 1], sc[x + 2], sc[x + 3]);
+            } else {
+#pragma unroll
+              for (int x = 0; x < G; ++x) lg[x] = sc[x];
+            }
+          }
+        }
 #pragma unroll
         for (int x = 0; x < G; ++x) {
-          float w = __shfl_sync(0xffffffffu, pw[x], (j8 + u) & 31);
-          if (j8 + u >= nk) w = 0.f;
+          const float bm = warp_max(live ? sc[x] : -INFINITY);
+          const float mn = fmaxf(m[x], bm);
+          const float pw = live ? ex2(sc[x] - mn) : 0.f;
+          const float f = ex2(m[x] - mn);  // 0 on the first block (m = -inf)
+          l[x] = l[x] * f + warp_sum(pw);
 #pragma unroll
-          for (int c = 0; c < DL; ++c) acc[x][c] = fmaf(w, vf[u][c], acc[x][c]);
+          for (int c = 0; c < DL / 2; ++c) acc[x][c] = __fmul2_rn(acc[x][c], make_float2(f, f));
+          m[x] = mn;
+          pwb[lane * G + x] = pw;
         }
       }
-    }
-  }
-  // merge the warps
+      // the K slot's reads are done: hand it to the copy engine again
+      __syncwarp();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(n + NS, false);
+      const bool vready =
+          __all_sync(0xffffffffu, bar_wait(saddr(vbar), (uint32_t)n & 1u, abort));
+      if (vready) v_landed = n + 1;
+      if (ready && vready && count > 0) {
+        auto vrow = [&](int rr, int off) {
+          float vf[DL];
+          lds_cols<T, DL>(vst + off, vf);
+          const float* w = pwb + rr * G;
 #pragma unroll
-  for (int x = 0; x < G; ++x) {
-    if (lane == 0) {
-      wml[(warp * G + x) * 2] = m[x];
-      wml[(warp * G + x) * 2 + 1] = l[x];
-    }
+          for (int x = 0; x < G; ++x) {
+            const float2 wx = make_float2(w[x], w[x]);
 #pragma unroll
-    for (int c = 0; c < DL; ++c) wacc[(warp * G + x) * D + lane * DL + c] = acc[x][c];
-  }
-  __syncthreads();
-  const size_t unit = (size_t)unit_i;
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    const int x = i / D, c = i % D;
-    float M = -INFINITY;
+            for (int c = 0; c < DL / 2; ++c)
+              acc[x][c] = __ffma2_rn(wx, make_float2(vf[2 * c], vf[2 * c + 1]), acc[x][c]);
+          }
+        };
+        int rr = 0;
+        for (; rr + 8 <= count; rr += 8) {
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wml[(w * G + x) * 2]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = wml[(w * G + x) * 2];
-        if (mw == -INFINITY) continue;
-        const float f = ex2(mw - M);
-        L += wml[(w * G + x) * 2 + 1] * f;
-        O += wacc[(w * G + x) * D + c] * f;
+          for (int u = 0; u < 8; ++u) vrow(rr + u, rr * 128 + voff[u]);
+        }
+        for (; rr < count; ++rr) vrow(rr, swz(rr, lane * DL * (int)sizeof(T)));
       }
+      // the V slot's reads are done: fetch the next block's V into it
+      __syncwarp();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(n + 1, true);
     }
-    p.part_o[unit * G * D + i] = O;
-    if (c == 0) p.part_ml[unit * G + x] = make_float2(M, L);
+    // merge the warps
+#pragma unroll
+    for (int x = 0; x < G; ++x) {
+      if (lane == 0) {
+        wml[(warp * G + x) * 2] = m[x];
+        wml[(warp * G + x) * 2 + 1] = l[x];
+      }
+#pragma unroll
+      for (int c = 0; c < DL / 2; ++c)
+        *reinterpret_cast<float2*>(wacc + (warp * G + x) * D + lane * DL + 2 * c) = acc[x][c];
+    }
+    __syncthreads();
+    const size_t unit = (size_t)unit_i;
+    const bool failed = *abort != 0;
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+      const int x = i / D, c = i % D;
+      float M = -INFINITY;
+      for (int w = 0; w < warps; ++w) M = fmaxf(M, wml[(w * G + x) * 2]);
+      float L = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+        for (int w = 0; w < warps; ++w) {
+          const float mw = wml[(w * G + x) * 2];
+          if (mw == -INFINITY) continue;
+          const float f = ex2(mw - M);
+          L += wml[(w * G + x) * 2 + 1] * f;
+          O += wacc[(w * G + x) * D + c] * f;
+        }
+      }
+      if (failed) M = __int_as_float(0x7fc00000);  // a stage never landed: the output reads NaN
+      p.part_o[unit * G * D + i] = O;
+      if (c == 0) p.part_ml[unit * G + x] = make_float2(M, L);
+    }
   }
+  // an aborting CTA lets the copies it issued land before it leaves
+  for (int r = k_landed; r < k_issued; ++r) {
+    const uint64_t t0 = global_ns();
+    while (!bar_test(saddr(&kbars[r % NS]), (uint32_t)(r / NS) & 1u) && global_ns() - t0 < kWaitNs) {
+    }
+  }
+  for (int r = v_landed; r < v_issued; ++r) {
+    const uint64_t t0 = global_ns();
+    while (!bar_test(saddr(vbar), (uint32_t)r & 1u) && global_ns() - t0 < kWaitNs) {
+    }
   }
 }
 
@@ -338,20 +527,119 @@ int sm_count() {
   return sms;
 }
 
+int max_smem_optin() {
+  static int v = 0;
+  if (v == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (v <= 0) v = 232448;
+  }
+  return v;
+}
+
+size_t smem_bytes(int warps, int stages, int D, int esize, int G) {
+  return 1024 +  // room to start the slots on a 1024-byte boundary
+         (size_t)warps * (stages + 1) * (slot_bytes(D, esize) + 8) +
+         ((size_t)G * D + (size_t)warps * kRows * G + (size_t)warps * G * 2 +
+          (size_t)warps * G * D) * sizeof(float) + 16;
+}
+
+using EncodeTiled = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(ptr);
+  }
+  return fn;
+}
+
+// Tensor map of a cache array [rows, heads, D]: boxes of 32 rows x 128 bytes
+// of one head, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int D, int esize, int heads, long long rows) {
+  EncodeTiled enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * esize, (cuuint64_t)D * esize * heads};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / esize), 1, (cuuint32_t)kRows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Warps per CTA and K slots per warp: the most warps (the math, not the
+// copies, sets the pace), then the most slots, that one CTA's shared memory
+// holds (one CTA per SM).
+bool kernel_shape(int D, int esize, int G, int& warps, int& stages) {
+  static const int cand[][2] = {{8, 3}, {8, 2}, {6, 2}, {4, 3}, {4, 2}, {2, 3}, {2, 2}, {1, 2}};
+  for (const auto& c : cand) {
+    if (smem_bytes(c[0], c[1], D, esize, G) <= (size_t)max_smem_optin()) {
+      warps = c[0];
+      stages = c[1];
+      return true;
+    }
+  }
+  return false;
+}
+
+// Rows per unit: a multiple of the CTA's 32 * warps rows (whole blocks for
+// every warp), at least kMinChunk, chosen so that the CTA with the most units
+// does the least work -- ceil(units / grid) * chunk is smallest (ties: the
+// longer chunk, fewer merges).
+int choose_chunk(const int* n, int nseq, int H_kv, int grid, int gran) {
+  int best = 0;
+  long long best_cost = -1;
+  for (int c = (kMinChunk + gran - 1) / gran * gran; c <= kMaxChunk; c += gran) {
+    long long units = 0;
+    for (int b = 0; b < nseq; ++b) units += (n[b] + c - 1) / c;
+    units *= H_kv;
+    const long long cost = (units + grid - 1) / grid * c;
+    if (best_cost < 0 || cost <= best_cost) {
+      best_cost = cost;
+      best = c;
+    }
+    if (units <= grid) break;  // longer chunks only lengthen every CTA's unit
+  }
+  return best;
+}
+
+// Kernel shape, chunk and the chunk index of every sequence, for row counts n.
+bool plan_units(Params& p, const int* n, int esize) {
+  if (!kernel_shape(p.d, esize, p.g, p.warps, p.stages)) return false;
+  const int gran = p.warps * kRows;
+  p.chunk = choose_chunk(n, p.nseq, p.H_kv, sm_count(), gran);
+  p.nbw = p.chunk / gran;
+  int chunks = 0;
+  for (int s = 0; s < p.nseq; ++s) {
+    p.seq[s].chunk0 = chunks;
+    chunks += (n[s] + p.chunk - 1) / p.chunk;
+  }
+  p.total_chunks = chunks;
+  return true;
+}
+
 template <typename T, int D, bool SH = false>
 cudaError_t launch_typed(const Params& p, cudaStream_t st) {
-  const size_t smem = ((size_t)p.g * D + kWarps * p.g * 2 + (size_t)kWarps * p.g * D) * sizeof(float);
+  const size_t smem = smem_bytes(p.warps, p.stages, D, (int)sizeof(T), p.g);
   const int units = p.total_chunks * p.H_kv;
+  CUtensorMap tm_k, tm_v;
+  if (!make_map(&tm_k, p.k, D, (int)sizeof(T), p.H_kv, p.rows_total) ||
+      !make_map(&tm_v, p.v, D, (int)sizeof(T), p.H_kv, p.rows_total))
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaSuccess;
   auto go = [&](auto kern) {
-    if (smem > 48 * 1024)
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    int per_sm = 0;
-    if (e == cudaSuccess)
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) {
-      const int grid = std::max(1, std::min(units, sm_count() * std::max(per_sm, 1)));
-      kern<<<grid, kThreads, smem, st>>>(p);
+      const int grid = std::max(1, std::min(units, sm_count()));
+      kern<<<grid, p.warps * 32, smem, st>>>(p, tm_k, tm_v);
       e = cudaGetLastError();
     }
   };
@@ -368,15 +656,6 @@ cudaError_t launch_typed(const Params& p, cudaStream_t st) {
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launches(2);
   return e;
-}
-
-// Keys per unit: about eight units per SM over the launch (the persistent
-// CTAs then finish within a fraction of a unit of each other), a multiple of
-// 32 in [kMinChunk, kMaxChunk].
-int chunk_for(long long total_rows, int H_kv, int sms) {
-  const long long want = (total_rows * H_kv + 8LL * sms - 1) / (8LL * sms);
-  const long long c = (want + 31) / 32 * 32;
-  return (int)std::min<long long>(kMaxChunk, std::max<long long>(kMinChunk, c));
 }
 
 int check(const snapkv_shape* sh, const int32_t* lens, int32_t layout, int32_t C) {
@@ -440,22 +719,24 @@ int launch_sh_attention(const ShAttention& a, void* stream) {
   p.sh_cap = a.cap;
   p.sh_logits = a.logits;
   p.sh_ml = a.ml;
+  p.rows_total = (long long)a.B * a.cap;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int sms = dec::sm_count();
   cudaError_t e = cudaSuccess;
   for (int g0 = 0; g0 < a.B && e == cudaSuccess; g0 += dec::kGroup) {
     const int g1 = std::min(a.B, g0 + dec::kGroup);
     p.nseq = g1 - g0;
     p.b0 = g0;
     // chunks sized for the full cache: the rows in use are only known on the device
-    p.chunk = dec::chunk_for((long long)p.nseq * a.cap, a.H_kv, sms);
-    const int per = (a.cap + p.chunk - 1) / p.chunk;
+    int caps[dec::kGroup];
     for (int s = 0; s < p.nseq; ++s) {
+      caps[s] = a.cap;
       p.seq[s].row0 = (long long)(g0 + s) * a.cap;
       p.seq[s].n = a.cap;
-      p.seq[s].chunk0 = s * per;
     }
-    p.total_chunks = p.nseq * per;
+    if (!dec::plan_units(p, caps, a.dtype == SNAPKV_BF16 ? 2 : 4)) {
+      e = cudaErrorInvalidValue;
+      break;
+    }
     if (p.dtype == SNAPKV_BF16)
       e = a.d == 64 ? dec::launch_typed<__nv_bfloat16, 64, true>(p, st)
                     : dec::launch_typed<__nv_bfloat16, 128, true>(p, st);
@@ -509,31 +790,30 @@ int snapkv_decode_attention(const snapkv_shape* shape, const void* q, const void
   p.k = k_cache;
   p.v = v_cache;
   p.out = out;
+  p.rows_total = 0;
+  for (int b = 0; b < shape->batch; ++b) p.rows_total += lens_host[b];
+  if (layout == SNAPKV_CACHE_SLOTS) p.rows_total = (long long)shape->batch * C;
   char* ws = static_cast<char*>(workspace);
   p.part_o = reinterpret_cast<float*>(ws);
   p.part_ml = reinterpret_cast<float2*>(
       ws + ((units_max * g * d * sizeof(float) + 255) & ~(size_t)255));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int sms = dec::sm_count();
   long long packed_row = 0;
   int result = SNAPKV_OK;
   for (int g0 = 0; g0 < shape->batch && result == SNAPKV_OK; g0 += dec::kGroup) {
     const int g1 = std::min(shape->batch, g0 + dec::kGroup);
-    long long rows = 0;
-    for (int b = g0; b < g1; ++b) rows += lens_host[b];
     p.nseq = g1 - g0;
     p.b0 = g0;
-    p.chunk = dec::chunk_for(rows, H_kv, sms);
-    int chunks = 0;
     for (int b = g0; b < g1; ++b) {
       dec::Seq& S = p.seq[b - g0];
       S.n = lens_host[b];
       S.row0 = layout == SNAPKV_CACHE_PACKED ? packed_row : (long long)b * C;
-      S.chunk0 = chunks;
-      chunks += (S.n + p.chunk - 1) / p.chunk;
       packed_row += S.n;
     }
-    p.total_chunks = chunks;
+    if (!dec::plan_units(p, lens_host + g0, shape->dtype == SNAPKV_BF16 ? 2 : 4)) {
+      result = SNAPKV_ERR_UNSUPPORTED;
+      break;
+    }
     cudaError_t e;
     if (p.dtype == SNAPKV_BF16)
       e = d == 64 ? dec::launch_typed<__nv_bfloat16, 64>(p, st)
