@@ -48,6 +48,7 @@
 #include <cstdint>
 #include <cstring>
 
+#include "pdl.cuh"
 #include "plan.h"
 #include "sh_attention.h"
 #include "snapkv.h"
@@ -261,7 +262,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     for (int s = 0; s <= NS; ++s)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(saddr(&kbars[s])) : "memory");
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  pdl_trigger();
   __syncthreads();
+  pdl_wait();  // the cache, the queries and the cache state are written
 
   // the rows [first, first + count) of block n of this warp's stream
   auto block_rows = [&](int n, int& seq, int& h, int& first, int& count) {
@@ -494,6 +497,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 // Grid (nseq, H_q), D threads: merges the chunks of one sequence and head.
 template <bool SH>
 __global__ void decode_combine(const __grid_constant__ Params p) {
+  pdl_trigger();
+  pdl_wait();  // every chunk's partials are written
   const int s = blockIdx.x, hq = blockIdx.y, c = threadIdx.x;
   const Seq& S = p.seq[s];
   const int h = hq / p.g, x = hq % p.g;
@@ -639,7 +644,8 @@ cudaError_t launch_typed(const Params& p, cudaStream_t st) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) {
       const int grid = std::max(1, std::min(units, sm_count()));
-      kern<<<grid, p.warps * 32, smem, st>>>(p, tm_k, tm_v);
+      e = launch_pdl(kern, dim3(grid), dim3(p.warps * 32), smem, st, p, tm_k, tm_v);
+      if (e == cudaSuccess) e = cudaGetLastError();
       e = cudaGetLastError();
     }
   };
@@ -652,8 +658,8 @@ cudaError_t launch_typed(const Params& p, cudaStream_t st) {
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  decode_combine<SH><<<dim3(p.nseq, p.H_q), D, 0, st>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(decode_combine<SH>, dim3(p.nseq, p.H_q), dim3(D), 0, st, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) count_launches(2);
   return e;
 }

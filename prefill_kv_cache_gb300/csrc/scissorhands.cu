@@ -33,6 +33,7 @@
 #include <cstdint>
 #include <vector>
 
+#include "pdl.cuh"
 #include "plan.h"
 #include "scissorhands.h"
 #include "sh_attention.h"
@@ -119,6 +120,8 @@ __global__ void __launch_bounds__(kThreads) sh_append_evict(const __grid_constan
   __shared__ int warp_tot[kThreads / 32];
   __shared__ int s_thr, s_need;
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();  // the previous step's state and history are written
   if (b == 0 && h == 0 && tid == 0) *a.done = 0;  // sh_mark's completion count
   const int n = a.state[b * 4], np = a.state[b * 4 + 2];
   if (n < 0 || n > a.budget) return;  // a cache that was never initialised
@@ -234,6 +237,8 @@ __global__ void __launch_bounds__(kThreads) sh_mark(const __grid_constant__ Args
   __shared__ float2 sml[G];
   __shared__ bool last;
   const int b = blockIdx.z, h = blockIdx.y, tid = threadIdx.x;
+  pdl_trigger();
+  pdl_wait();  // the logits and each query head's (max, sum) are written
   int n = a.state[b * 4] + 1;
   if (n > a.budget) n -= a.evict;
   n = min(max(n, 0), a.cap);
@@ -449,8 +454,10 @@ int scissorhands_step(const snapkv_shape* shape, const scissorhands_params* para
       cudaFuncSetAttribute(sh::sh_append_evict, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
     return SNAPKV_ERR_CUDA;
-  sh::sh_append_evict<<<dim3(a.H_kv, a.B), sh::kThreads, smem, s>>>(a);
-  if (cudaGetLastError() != cudaSuccess) return SNAPKV_ERR_CUDA;
+  if (launch_pdl(sh::sh_append_evict, dim3(a.H_kv, a.B), dim3(sh::kThreads), smem, s, a) !=
+          cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return SNAPKV_ERR_CUDA;
 
   ShAttention at{};
   at.B = a.B;
@@ -473,14 +480,15 @@ int scissorhands_step(const snapkv_shape* shape, const scissorhands_params* para
   if (launch_sh_attention(at, stream) != cudaSuccess) return SNAPKV_ERR_CUDA;
 
   const dim3 grid((a.cap + sh::kThreads - 1) / sh::kThreads, a.H_kv, a.B);
+  cudaError_t e;
   switch (a.H_q / a.H_kv) {
-    case 1: sh::sh_mark<1><<<grid, sh::kThreads, 0, s>>>(a); break;
-    case 2: sh::sh_mark<2><<<grid, sh::kThreads, 0, s>>>(a); break;
-    case 4: sh::sh_mark<4><<<grid, sh::kThreads, 0, s>>>(a); break;
-    case 8: sh::sh_mark<8><<<grid, sh::kThreads, 0, s>>>(a); break;
-    default: sh::sh_mark<16><<<grid, sh::kThreads, 0, s>>>(a); break;
+    case 1: e = launch_pdl(sh::sh_mark<1>, grid, dim3(sh::kThreads), 0, s, a); break;
+    case 2: e = launch_pdl(sh::sh_mark<2>, grid, dim3(sh::kThreads), 0, s, a); break;
+    case 4: e = launch_pdl(sh::sh_mark<4>, grid, dim3(sh::kThreads), 0, s, a); break;
+    case 8: e = launch_pdl(sh::sh_mark<8>, grid, dim3(sh::kThreads), 0, s, a); break;
+    default: e = launch_pdl(sh::sh_mark<16>, grid, dim3(sh::kThreads), 0, s, a); break;
   }
-  if (cudaGetLastError() != cudaSuccess) return SNAPKV_ERR_CUDA;
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return SNAPKV_ERR_CUDA;
   count_launches(2);
   return SNAPKV_OK;
 }
