@@ -16,7 +16,9 @@ on the launching stream), the end-to-end figure through the host-buffer entry
 point (host->device copies of the inputs and device->host copies of the
 compressed cache inside the timed region), the oracle timed on host cores on
 a bounded sample, SM clocks and throttle reasons sampled during the timed
-region, and the number of library kernels launched in it.
+region, and the number of library kernels launched in it; after the timed
+region, decode steps over the full and the compressed cache, and decode steps
+with Scissorhands eviction starting from the compressed cache.
 
 `--impl reference` times the CPU oracle instead, on the same workload.
 """
@@ -51,6 +53,9 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=None, help="override the layer count")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-scissorhands", action="store_true")
+    ap.add_argument("--case", choices=["decode", "scissorhands"], default=None,
+                    help="run a small fixed case for a profiler and exit (no timing)")
     return ap.parse_args()
 
 
@@ -206,6 +211,9 @@ def main():
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
+    if args.case:
+        profile_case(args.case)
+        return
 
     import torch
     import torch.distributed as dist
@@ -311,6 +319,9 @@ def main():
             traffic = None
 
     decode = decode_step(S, torch, data, outs, seqlens, cfg, dev, stream, peak)
+    sh_decode = None
+    if not args.no_scissorhands:
+        sh_decode = scissorhands_decode(torch, outs, seqlens, cfg, dev, stream, peak)
 
     e2e = None
     if not args.no_e2e:
@@ -344,12 +355,42 @@ def main():
             "cpu_baseline": cpu,
             "e2e": e2e,
             "decode": decode,
+            "scissorhands": sh_decode,
             "gpu_launches": launches,
             "clocks": clk,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def profile_case(name: str) -> None:
+    """Small fixed cases for ncu (a few hundred MB on the device, a handful of
+    launches): 'decode' = four decode steps over one 131072-token Llama-3-8B
+    layer cache; 'scissorhands' = 40 Scissorhands steps (budget 4096, r = 10,
+    w = 400, batches of 2048) of one layer starting from a full cache, so the
+    first step evicts."""
+    import torch
+
+    from prefill_kv_cache_gb300 import scissorhands as SH
+    from prefill_kv_cache_gb300 import snapkv as S
+
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1)
+    rnd = lambda *shape: torch.randn(shape, generator=g, device="cuda").to(torch.bfloat16)
+    if name == "decode":
+        L = 131072
+        k, v, q = rnd(L, 8, 128), rnd(L, 8, 128), rnd(1, 32, 128)
+        for _ in range(4):
+            S.decode_attention(q, k, v, [L], S.CACHE_PACKED)
+    else:
+        c = SH.Cache(1, 32, 8, 128, torch.bfloat16, SH.Params(budget=4096))
+        c.init([4096], [131072], rnd(1, 4096, 8, 128), rnd(1, 4096, 8, 128))
+        q, kn, vn = rnd(1, 32, 128), rnd(1, 8, 128), rnd(1, 8, 128)
+        for _ in range(40):
+            c.step(q, kn, vn)
+    torch.cuda.synchronize()
+    print(f"case {name}: ok")
 
 
 def replica_ms(ms_local: float, world: int, dev) -> float:
@@ -428,6 +469,77 @@ def decode_step(S, torch, data, outs, seqlens, cfg, dev, stream, peak, reps=5):
     res["note"] = ("one query token per sequence, all layers back to back in one CUDA graph; "
                    "K and V bytes read once per layer are the roofline bytes")
     return res
+
+
+def scissorhands_decode(torch, outs, seqlens, cfg, dev, stream, peak):
+    """Decode steps with Scissorhands eviction (scissorhands_step) through
+    every layer, each layer's cache starting from the compressed cache the
+    timed compression wrote, with the settings of the Scissorhands page:
+    budget = C, r = 10, w = 400, batches of C / 2.  One step of all layers is
+    captured in a CUDA graph; the state lives on the device, so each replay is
+    the next decode step.  Timed: the first step (the cache starts full, so it
+    evicts) and then one whole eviction period of C / 2 steps."""
+    from prefill_kv_cache_gb300 import scissorhands as SH
+
+    B = len(seqlens)
+    H_q, H_kv, d, C = cfg["H_q"], cfg["H_kv"], cfg["d"], cfg["C"]
+    dt = outs[0][0].dtype
+    prm = SH.Params(budget=C, recent=10, history=400, evict=C // 2)
+    caches = [SH.Cache(B, H_q, H_kv, d, dt, prm, device=dev) for _ in outs]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(78)
+    qs, ks, vs = ([torch.randn((B, n, d), generator=gen, device=dev).to(dt) for _ in outs]
+                  for n in (H_q, H_kv, H_kv))
+    out = torch.empty((B, H_q, d), dtype=torch.float32, device=dev)
+    lens_c = [min(int(L), C) for L in seqlens]
+
+    def init():
+        for c, (ok, ov, oi) in zip(caches, outs):
+            c.init(lens_c, seqlens, ok, ov, oi, stream=stream)
+
+    def sweep(st):
+        for c, q, k, v in zip(caches, qs, ks, vs):
+            c.step(q, k, v, out=out, stream=st)
+
+    init()
+    for _ in range(3):
+        sweep(stream)
+    torch.cuda.synchronize()
+    cap = torch.cuda.Stream(device=dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        sweep(cap)
+    init()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    period = prm.c().evict
+    ev[0].record()
+    graph.replay()
+    ev[1].record()
+    for _ in range(period):
+        graph.replay()
+    ev[2].record()
+    torch.cuda.synchronize()
+    layers = len(outs)
+    n = list(lens_c)
+    rows = []
+    for t in range(period + 1):
+        n = [x + 1 - (period if x + 1 > C else 0) for x in n]
+        if t > 0:
+            rows.append(sum(n))
+    rows_mean = statistics.mean(rows)
+    us_first = 1e3 * ev[0].elapsed_time(ev[1]) / layers
+    us_mean = 1e3 * ev[1].elapsed_time(ev[2]) / period / layers
+    nbytes = 2 * rows_mean * H_kv * d * outs[0][0].element_size()
+    return {
+        "budget": C, "recent": 10, "history": 400, "evict": period,
+        "us_per_layer_step": us_mean, "us_per_layer_evicting_step": us_first,
+        "rows_mean": rows_mean, "gbs": nbytes / us_mean / 1e3,
+        "frac": nbytes / us_mean / 1e3 / peak,
+        "note": ("mean over one eviction period (the last step evicts), all layers back to "
+                 "back in one CUDA graph; the K and V bytes of the rows attended are the "
+                 "roofline bytes"),
+    }
 
 
 def run_e2e(S, torch, data, seqlens, cfg, shape, dev, stream, args, layers):
