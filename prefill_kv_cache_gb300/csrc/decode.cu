@@ -495,26 +495,58 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 }
 
 // Grid (nseq, H_q), D threads: merges the chunks of one sequence and head.
+// Every chunk's (max, sum) is read once, all chunks at a time across the
+// threads; their scale factors go to shared memory; each thread then sums
+// its column over the chunks with independent loads.
+constexpr int kCombineTile = 1024;  // chunks whose scale factors sit in shared memory at once
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, w) : v + w;
+  }
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();  // red is free
+  if ((threadIdx.x & 31) == 0) red[warp] = v;
+  __syncthreads();
+  v = red[0];
+  for (int w = 1; w < nw; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+  return v;
+}
+
 template <bool SH>
 __global__ void decode_combine(const __grid_constant__ Params p) {
+  __shared__ float fk[kCombineTile];
+  __shared__ float red[32];
   pdl_trigger();
   pdl_wait();  // every chunk's partials are written
   const int s = blockIdx.x, hq = blockIdx.y, c = threadIdx.x;
   const Seq& S = p.seq[s];
   const int h = hq / p.g, x = hq % p.g;
   const int nch = (S.n + p.chunk - 1) / p.chunk;
+  const size_t ustride = (size_t)p.H_kv * p.g;                       // between chunks
+  const float2* ml = p.part_ml + ((size_t)S.chunk0 * p.H_kv + h) * p.g + x;  // chunk k: ml[k * ustride]
+  const float* po = p.part_o + (((size_t)S.chunk0 * p.H_kv + h) * p.g + x) * p.d + c;
   float M = -INFINITY;
-  for (int k = 0; k < nch; ++k)
-    M = fmaxf(M, p.part_ml[((size_t)(S.chunk0 + k) * p.H_kv + h) * p.g + x].x);
-  float L = 0.f, O = 0.f;
-  for (int k = 0; k < nch; ++k) {
-    const size_t unit = (size_t)(S.chunk0 + k) * p.H_kv + h;
-    const float2 ml = p.part_ml[unit * p.g + x];
-    if (ml.x == -INFINITY) continue;
-    const float f = ex2(ml.x - M);
-    L += ml.y * f;
-    O += p.part_o[(unit * p.g + x) * p.d + c] * f;
+  for (int k = c; k < nch; k += blockDim.x) M = fmaxf(M, ml[(size_t)k * ustride].x);
+  M = block_reduce(M, true, red);
+  float Lp = 0.f, O = 0.f;
+  for (int k0 = 0; k0 < nch; k0 += kCombineTile) {
+    const int nk = min(kCombineTile, nch - k0);
+    __syncthreads();  // the previous tile's factors are read
+    for (int k = c; k < nk; k += blockDim.x) {
+      const float2 v = ml[(size_t)(k0 + k) * ustride];
+      const float f = v.x == -INFINITY ? 0.f : ex2(v.x - M);
+      fk[k] = f;
+      Lp += v.y * f;
+    }
+    __syncthreads();
+    const float* pk = po + (size_t)k0 * ustride * p.d;
+#pragma unroll 8
+    for (int k = 0; k < nk; ++k) O = fmaf(pk[(size_t)k * ustride * p.d], fk[k], O);
   }
+  const float L = block_reduce(Lp, false, red);
   p.out[((size_t)(p.b0 + s) * p.H_q + hq) * p.d + c] = O / L;
   if constexpr (SH) {
     if (c == 0) p.sh_ml[(size_t)(p.b0 + s) * p.H_q + hq] = make_float2(M, L);
