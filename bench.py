@@ -145,6 +145,34 @@ def workload_bytes(cfg, seqlens, esz):
     return score, score + gather
 
 
+# exp2 per clock per SM of the special-function units, measured on GB300 (an
+# in-bounds throughput probe, matching ncu's XU pipe counter)
+MUFU_EX2_PER_CLK_SM = 32
+
+
+def score_work(cfg, seqlens):
+    """Tensor-core flops and exp2 count of one layer's two-pass scoring: per
+    scored sequence (L > C) and KV head, pass 1 forms the W*g window rows'
+    logits against all L keys and pass 2 against the P = L - W prefix keys;
+    each logit is 2 d flops of bf16 MMA and one exp2."""
+    Wp = cfg["W"] * cfg["H_q"] // cfg["H_kv"]
+    keys = sum(L + (L - cfg["W"]) for L in seqlens if L > cfg["C"])
+    return 2 * Wp * cfg["d"] * keys * cfg["H_kv"], Wp * keys * cfg["H_kv"]
+
+
+def compute_peaks(sms: int):
+    """(bf16 TFLOP/s, its kind, exp2 per second in 1e12, its kind)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            mp = json.load(f)
+        tc, tc_kind = float(mp["bf16_tflops"]), "measured (burst)"
+        mhz = float(mp.get("sm_max_mhz", 2070.0))
+    except Exception:
+        tc, tc_kind, mhz = 1900.0, "fallback", 2070.0
+    mufu = MUFU_EX2_PER_CLK_SM * sms * mhz * 1e6 / 1e12
+    return tc, tc_kind, mufu, f"derived: {MUFU_EX2_PER_CLK_SM} ex2/clk/SM x {sms} SMs x {mhz:.0f} MHz"
+
+
 def cpu_baseline(name, layers_total, nthreads=None, lay=None, min_seconds=10.0, max_layers=4):
     """Oracle on whole layers (all KV heads), layer 0 onwards, until about
     min_seconds of CPU time are spent (at most max_layers): a bounded sample."""
@@ -306,6 +334,10 @@ def main():
     score_bytes, compress_bytes = workload_bytes(cfg, seqlens, esz)
     peak, peak_kind = hbm_peak()
     achieved = score_bytes / (score_avg_ms / 1e3) / 1e9
+    flops, exps = score_work(cfg, seqlens)
+    tc_peak, tc_kind, mufu_peak, mufu_kind = compute_peaks(
+        torch.cuda.get_device_properties(dev).multi_processor_count)
+    tensor_cores = cfg["dtype"] == "bf16" and cfg["W"] * H_q // H_kv in (128, 256)
     compress_gbs = compress_bytes / (ms / layers / 1e3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "score_kernel_traffic.json")
@@ -352,6 +384,17 @@ def main():
                          "bytes_per_launch": score_bytes},
             "roofline_compress": {"achieved": compress_gbs, "peak": peak, "unit": "GB/s",
                                   "frac": compress_gbs / peak, "bytes_per_layer": compress_bytes},
+            # the same launch against its compute ceilings (two passes recompute the logits)
+            "roofline_tensor": None if not tensor_cores else {
+                "bound": "tensor", "achieved": flops / (score_avg_ms / 1e3) / 1e12,
+                "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": flops / (score_avg_ms / 1e3) / 1e12 / tc_peak,
+                "flops_per_launch": flops, "peak_kind": tc_kind},
+            "roofline_mufu": {
+                "bound": "alu", "achieved": exps / (score_avg_ms / 1e3) / 1e12,
+                "peak": mufu_peak, "unit": "T exp2/s",
+                "frac": exps / (score_avg_ms / 1e3) / 1e12 / mufu_peak,
+                "exp2_per_launch": exps, "peak_kind": mufu_kind},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "decode": decode,
