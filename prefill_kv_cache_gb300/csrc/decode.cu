@@ -15,23 +15,28 @@
 // on the CUDA cores (split-K "flash decoding"), with the cache streamed
 // through shared memory by the bulk-copy (TMA) engine:
 //
-//   decode_chunk   persistent, one CTA per SM; work units are (key chunk,
-//                  KV head).  Each warp owns a contiguous share of a unit's
-//                  rows and streams it in blocks of 32 rows through its own
-//                  ring of shared-memory stages: one lane issues the TMA
-//                  tensor copies of the block's K and V (boxes of 32 rows x
-//                  128 bytes, 128-byte swizzle), which complete on the
-//                  stage's mbarrier, and the next stages are in flight while
-//                  the current one is computed -- blocks of the next unit
-//                  included.  The swizzle puts the 16-byte pieces of 8
-//                  consecutive rows in distinct banks, so the per-lane row
-//                  reads of the logit phase are conflict-free.  Lane i
-//                  computes row i's logits for the
-//                  g query heads of the group; the warp updates its running
-//                  max and sum of exp2; each lane then accumulates its d/32
-//                  columns over the block's V rows.  The CTA merges its warps
-//                  and writes (max, sum, unnormalised output) per query head.
+//   decode_chunk   persistent, one CTA of up to 8 warps per SM; work units
+//                  are (key chunk, KV head), the chunk length chosen so the
+//                  CTA with the most units does the least work.  Each warp
+//                  owns a contiguous share of a unit's rows and streams it in
+//                  blocks of 32 rows through its own shared-memory slots --
+//                  two for K, one for V: lane 0 issues the TMA tensor copies
+//                  (boxes of 32 rows x 128 bytes of one head, 128-byte
+//                  swizzle) that complete on each slot's mbarrier; the next
+//                  block's K is in flight while the current block is
+//                  computed, its V while the next block's logits are (blocks
+//                  of the next unit included).  The swizzle puts the 16-byte
+//                  pieces of 8 consecutive rows in distinct banks, so the
+//                  per-lane row reads of the logit phase are conflict-free.
+//                  Lane i computes row i's logits for the g query heads of
+//                  the group; the warp updates its running max and sum of
+//                  exp2; each lane then accumulates its d/32 columns over the
+//                  block's V rows (packed fp32x2 FMAs in both phases).  The
+//                  CTA merges its warps and writes (max, sum, unnormalised
+//                  output) per query head.
 //   decode_combine grid (B, H_q): merges the chunks of each sequence.
+//
+// Both are launched with programmatic dependent launch (pdl.cuh).
 //
 // The Scissorhands instantiation (SH = true) serves one step of the
 // decode-time eviction in scissorhands.cu: the rows of each sequence come from
