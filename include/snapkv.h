@@ -25,6 +25,10 @@
  *     the W window rows, plus their positions (glossary, step 4: decode uses
  *     the compressed cache).  When L <= C every position is kept.
  *
+ * The same library also runs decode steps over a cache (snapkv_decode_attention
+ * below) and Scissorhands decode-time eviction over a budgeted cache that can
+ * start from the compressed one (scissorhands.h).
+ *
  * The parameter names of the glossary's usage example map as follows:
  * window_size -> W, max_capacity_prompt -> C, kernel_size -> kernel_size,
  * pooling ("avgpool" / "maxpool") -> pool_type.
