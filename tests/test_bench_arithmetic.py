@@ -1,6 +1,7 @@
-"""The benchmark's roofline arithmetic against the per-workload figures of the
-scope table (algorithmic bytes; MMA flops and exp counts of the two passes).
-CPU only."""
+"""The benchmark's roofline arithmetic against figures worked out by hand from
+the workload shapes: algorithmic bytes (K once, the window queries, the
+gathered K / V rows read and written, the indices) and the MMA flops and exp
+counts of the two score passes.  CPU only."""
 import pytest
 
 import bench
