@@ -118,3 +118,32 @@ def test_decode_full_size_128k(layout):
                            layout, C)
     ref = oracle.decode_attention(q, ks, vs)
     _check(o.cpu().numpy(), ref, np.abs(synth.bf16_to_f32(vs[0])).max())
+
+
+@pytest.mark.parametrize("layout", [S.CACHE_PACKED, S.CACHE_SLOTS])
+def test_decode_more_sequences_than_one_launch_group(layout):
+    """1100 sequences: three launch groups of at most 512 sequences run in
+    turn and share one workspace."""
+    lens = [int(x) for x in np.random.default_rng(61).integers(1, 48, 1100)]
+    H_q, H_kv, d = 8, 2, 64
+    k, v = _cache(62, lens, H_kv, d, "bf16")
+    q = _q(63, len(lens), H_q, d, "bf16")
+    offs = np.concatenate([[0], np.cumsum(lens)])
+    ks = [k[offs[b]:offs[b + 1]] for b in range(len(lens))]
+    vs = [v[offs[b]:offs[b + 1]] for b in range(len(lens))]
+    C = 48
+    if layout == S.CACHE_SLOTS:
+        kc = np.zeros((len(lens), C, H_kv, d), dtype=k.dtype)
+        vc = np.zeros((len(lens), C, H_kv, d), dtype=v.dtype)
+        for b in range(len(lens)):
+            kc[b, :lens[b]] = ks[b]
+            vc[b, :lens[b]] = vs[b]
+    else:
+        kc, vc = k, v
+    launches = S.kernel_launches()
+    o = S.decode_attention(parity.to_device(q), parity.to_device(kc), parity.to_device(vc), lens,
+                           layout, C)
+    torch.cuda.synchronize()
+    assert S.kernel_launches() - launches == 2 * 3
+    ref = oracle.decode_attention(q, ks, vs)
+    _check(o.cpu().numpy(), ref, max(np.abs(synth.bf16_to_f32(x)).max() for x in vs))

@@ -265,3 +265,33 @@ def test_graph_replay_matches_eager():
         np.testing.assert_array_equal(a["hist"][bb, :, :, :n], b["hist"][bb, :, :, :n])
         np.testing.assert_array_equal(a["k"][bb, :n], b["k"][bb, :n])
         np.testing.assert_array_equal(a["v"][bb, :n], b["v"][bb, :n])
+
+
+def test_more_sequences_than_one_launch_group():
+    """600 sequences (the attention runs as two launch groups): under uniform
+    attention every sequence's cache must be the newest tokens, with the
+    budget, the batch size and each sequence's starting length respected."""
+    B, H_kv, g, d, dtype = 600, 2, 2, 64, torch.bfloat16
+    c = SH.Cache(B, H_kv * g, H_kv, d, dtype, SH.Params(budget=8, recent=2, history=3, evict=4))
+    rng = np.random.default_rng(70)
+    k0, v0, pos0 = _prefix(rng, B, 8, H_kv, d, dtype)
+    lens0 = [int(x) for x in rng.integers(0, 9, B)]
+    nxt = [1000 + 7 * b for b in range(B)]
+    c.init(lens0, nxt, _dev(k0, dtype), _dev(v0, dtype), torch.from_numpy(pos0).cuda())
+    zeros = torch.zeros((B, H_kv * g, d), dtype=dtype, device="cuda")
+    steps = 6
+    for _ in range(steps):
+        kn = _dev(_rand(rng, (B, H_kv, d), dtype), dtype)
+        c.step(zeros, kn, kn)
+    snap = snapshot(c)
+    for b in range(B):
+        n = lens0[b]
+        stream = list(range(nxt[b], nxt[b] + steps))
+        for _ in range(steps):
+            n += 1
+            if n > 8:
+                n -= 4
+        assert list(snap["state"][b, :3]) == [n, steps, nxt[b] + steps]
+        for h in range(H_kv):
+            arrived = list(pos0[b, h, :lens0[b]]) + stream
+            assert list(snap["pos"][b, h, :n]) == arrived[-n:], (b, h)
