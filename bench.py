@@ -12,7 +12,8 @@ C = 4096).  Each layer's K and V (537 MB) are far larger than L2, so no L2
 flush is needed between iterations.
 
 Also reported: the score kernel alone against the HBM roofline (CUDA events
-on the launching stream), the end-to-end figure through the host-buffer entry
+on the launching stream) and, beside it, against its tensor-core and exp2
+ceilings (two passes recompute the logits), the end-to-end figure through the host-buffer entry
 point (host->device copies of the inputs and device->host copies of the
 compressed cache inside the timed region), the oracle timed on host cores on
 a bounded sample, SM clocks and throttle reasons sampled during the timed
