@@ -279,6 +279,21 @@ int snapkv_compress_host(const snapkv_shape *shape, const void *q_win_host,
 uint64_t snapkv_kernel_launches(void);
 
 /*
+ * Which scoring path ran.  Scoring runs on the 5th-generation tensor cores
+ * (one tcgen05 kernel) for bf16 with d in {64, 128} and W * g in {128, 256},
+ * and on the CUDA cores (FFMA kernels) for every other supported shape; the
+ * choice depends on the shape only, never on a runtime condition.  This
+ * returns how many scoring launches (one per sweep over K that produces the
+ * scores) the process has made on `path` so far, all devices and streams:
+ * SNAPKV_SCORE_PATH_TENSOR_CORES or SNAPKV_SCORE_PATH_CUDA_CORES; 0 for any
+ * other value.
+ */
+#define SNAPKV_SCORE_PATH_TENSOR_CORES 0
+#define SNAPKV_SCORE_PATH_CUDA_CORES 1
+
+uint64_t snapkv_score_path_launches(int32_t path);
+
+/*
  * snapkv_compress without a caller-provided workspace.  The SnapKV pages have
  * no counterpart to this entry point; it exists for callers that cannot call
  * cudaMalloc -- for example a plugin inside a serving engine whose device
@@ -293,17 +308,30 @@ uint64_t snapkv_kernel_launches(void);
  * SNAPKV_ERR_WORKSPACE before anything is enqueued (one Llama-3-8B-shaped
  * layer of 131072 tokens needs about 10.5 MB).  The call allocates nothing.
  *
- * The first call on a device looks up the array's device address (a CUDA
- * runtime query, made once per device with that device current); make that
- * first call before any stream capture.  All calls share the one array and
- * it keeps the last call's contents: calls that may overlap on the GPU (other
- * streams, other host threads) race on it and must be serialised by the
- * caller.  snapkv_get_status does not apply to this entry point.
+ * Every call looks up the array's device address in the calling thread's
+ * current CUDA context (a runtime query that allocates nothing), so a context
+ * switch or a cudaDeviceReset between calls is safe.  The first call in a
+ * context may load the library's device code: make it before any stream
+ * capture.  All calls in a context share the one array and it keeps the last
+ * call's contents: calls that may overlap on the GPU (other streams, other
+ * host threads) race on it and must be serialised by the caller.
+ * snapkv_get_status does not apply to this entry point; use
+ * snapkv_noalloc_get_status.
  */
 int snapkv_compress_noalloc(const snapkv_shape *shape, const void *q_win, const void *k,
                             const void *v, const int32_t *seqlens_host, int32_t W,
                             int32_t kernel_size, int32_t pool_type, int32_t C, void *out_k,
                             void *out_v, int32_t *out_idx, void *stream);
+
+/*
+ * Synchronize `stream`, then read the status word that the kernels of the
+ * last snapkv_compress_noalloc in the current context wrote into the
+ * built-in scratch: SNAPKV_OK, or SNAPKV_ERR_TIMEOUT if a bounded device-side
+ * wait gave up (the outputs of that call are then incomplete).  Like the
+ * entry point it serves, the SnapKV pages have no counterpart.  Returns
+ * SNAPKV_ERR_CUDA if the synchronize or the read fails.
+ */
+int snapkv_noalloc_get_status(void *stream);
 
 /*
  * ---- Decode step over a KV cache ----

@@ -559,25 +559,13 @@ __global__ void decode_combine(const __grid_constant__ Params p) {
 }
 
 int sm_count() {
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 148;
-  }
-  return sms;
+  const DeviceInfo* di = current_device_info();
+  return di ? di->sms : 148;
 }
 
 int max_smem_optin() {
-  static int v = 0;
-  if (v == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (v <= 0) v = 232448;
-  }
-  return v;
+  const DeviceInfo* di = current_device_info();
+  return di ? di->smem_optin : 232448;
 }
 
 size_t smem_bytes(int warps, int stages, int D, int esize, int G) {

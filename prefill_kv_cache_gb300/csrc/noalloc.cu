@@ -10,8 +10,6 @@
 // from differs.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "snapkv.h"
 
 namespace snapkv {
@@ -23,26 +21,15 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 
 static __device__ __align__(256) unsigned char g_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_scratch on the current device, looked up once per
-// device (in host code the array's name is only a stand-in for the symbol).
-cudaError_t scratch_for_current_device(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
-  return cudaSuccess;
+// Device address of g_scratch in the calling thread's current context.  In
+// host code the array's name is only a stand-in for the symbol, never a
+// device address.  Each CUDA context has its own copy of the array, so the
+// address is looked up on every call rather than cached: a cached value would
+// go stale after cudaDeviceReset or point into another context when the
+// caller switches contexts.  The lookup allocates nothing; the first one in a
+// context may load the library's device code.
+cudaError_t scratch_in_current_context(void** out) {
+  return cudaGetSymbolAddress(out, g_scratch);
 }
 
 }  // namespace
@@ -63,10 +50,23 @@ extern "C" int snapkv_compress_noalloc(const snapkv_shape* shape, const void* q_
   }
   if (need > kNoAllocScratchBytes) return SNAPKV_ERR_WORKSPACE;
   void* scratch = nullptr;
-  if (scratch_for_current_device(&scratch) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  if (scratch_in_current_context(&scratch) != cudaSuccess) return SNAPKV_ERR_CUDA;
   // The status word and the work-queue counters at the start of the scratch
   // are cleared on the stream by snapkv_compress; every other region is fully
   // written before it is read, so the previous call's contents do not matter.
   return snapkv_compress(shape, q_win, k, v, seqlens_host, W, kernel_size, pool_type, C, out_k,
                          out_v, out_idx, scratch, kNoAllocScratchBytes, stream);
+}
+
+extern "C" int snapkv_noalloc_get_status(void* stream) {
+  using namespace snapkv;
+  // the status word sits at the start of the scratch, where the workspace
+  // layout puts it
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SNAPKV_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_scratch, sizeof(int), 0, cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return SNAPKV_ERR_CUDA;
+  return word == 0 ? SNAPKV_OK : SNAPKV_ERR_TIMEOUT;
 }

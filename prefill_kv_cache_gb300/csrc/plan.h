@@ -70,6 +70,23 @@ struct Plan {
 // Adds n to the library's process-wide kernel-launch counter.
 void count_launches(int n);
 
+// Per-path count of scoring launches (one per pass-2 sweep over K): the
+// tcgen05 kernel or the CUDA-core kernels.  Values match snapkv.h's
+// SNAPKV_SCORE_PATH_* constants.
+constexpr int kScorePathTensorCores = 0;
+constexpr int kScorePathCudaCores = 1;
+void count_score_launches(int path, int n);
+
+// Attributes of the calling thread's current device, looked up once per
+// device under a lock: concurrent first calls from several host threads are
+// safe, and a process that drives GPUs of different kinds plans each launch
+// with its own device's values.  Null if the query fails.
+struct DeviceInfo {
+  int sms;         // streaming multiprocessors
+  int smem_optin;  // largest dynamic shared memory per block (opt-in), bytes
+};
+const DeviceInfo* current_device_info();
+
 // Launchers (each returns a cudaError_t as int).
 int launch_score_simt(const Plan& p, void* stream);
 int launch_select_gather(const Plan& p, void* stream);

@@ -236,6 +236,7 @@ static int launch_simt_typed(const Plan& p, cudaStream_t st) {
   }
   score_pass2_simt<T, D><<<p.total_pieces, kSimtThreads, smem, st>>>(p);
   count_launches(1);
+  count_score_launches(kScorePathCudaCores, 1);
   return cudaGetLastError();
 }
 

@@ -229,6 +229,88 @@ __device__ __forceinline__ void row_sum_members(const float* v, const float* lse
   }
 }
 
+// Packed fp32x2 arithmetic (one instruction for two lanes of values).
+__device__ __forceinline__ uint64_t pk(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk(uint64_t x, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t ex2x2(uint64_t x) {
+  float a, b;
+  upk(x, a, b);
+  return pk(ex2(a), ex2(b));
+}
+__device__ __forceinline__ float sum4(const uint64_t (&a)[4]) {
+  float x0, x1, x2, x3, x4, x5, x6, x7;
+  upk(a[0], x0, x1);
+  upk(a[1], x2, x3);
+  upk(a[2], x4, x5);
+  upk(a[3], x6, x7);
+  return ((x0 + x1) + (x2 + x3)) + ((x4 + x5) + (x6 + x7));
+}
+
+// Pass 2, one 32-column chunk of a key's row of logits: adds
+// exp2(v[j] * c2 - lse2[j]) into four pair accumulators (pair p of the chunk
+// goes to acc[p % 4], so acc[k] holds the columns 2k, 2k+1 mod 8).  nl holds
+// -lse2 of the chunk's 32 query rows (shared memory, 16-byte aligned).
+__device__ __forceinline__ void p2_chunk(const uint32_t* v, const float* nl, uint64_t c2c2,
+                                         uint64_t (&acc)[4]) {
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    const float4 l4 = *reinterpret_cast<const float4*>(nl + j);
+    const uint64_t x0 =
+        fma2(pk(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), c2c2, pk(l4.x, l4.y));
+    const uint64_t x1 =
+        fma2(pk(__uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])), c2c2, pk(l4.z, l4.w));
+    acc[(j >> 1) & 3] = add2(acc[(j >> 1) & 3], ex2x2(x0));
+    acc[((j >> 1) + 1) & 3] = add2(acc[((j >> 1) + 1) & 3], ex2x2(x1));
+  }
+}
+
+// Pass 1, one 32-key chunk of a query row, all keys visible: the sum of
+// exp2(v[j] * c2 - M) for the row's running reference M.
+__device__ __forceinline__ float p1_chunk_sum(const uint32_t* v, uint64_t c2c2, uint64_t nMnM) {
+  uint64_t a[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int j = 0; j < 32; j += 2)
+    a[(j >> 1) & 3] = add2(
+        a[(j >> 1) & 3],
+        ex2x2(fma2(pk(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), c2c2, nMnM)));
+  return sum4(a);
+}
+
+// Pass 1, one 32-key chunk with an exact reference: keys past `limit` (the
+// last key the row sees, relative to the chunk) are masked; the running
+// (M, Z) move to the larger of M and the chunk's largest scaled logit.
+__device__ __forceinline__ void p1_chunk_exact(uint32_t* v, int limit, float c2, float& M,
+                                               float& Z) {
+  float tmax = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float x = j > limit ? -INFINITY : __uint_as_float(v[j]);
+    v[j] = __float_as_uint(x);
+    tmax = fmaxf(tmax, x);
+  }
+  if (tmax == -INFINITY) return;  // the row sees no key of this chunk
+  const float Mn = fmaxf(M, tmax * c2);
+  const float z = p1_chunk_sum(v, pk(c2, c2), pk(-Mn, -Mn));
+  Z = Z * ex2(M - Mn) + z;  // M = -inf: ex2 gives 0 and Z was 0
+  M = Mn;
+}
+
 // ------------------------------------------------------------ schedule ---
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -298,9 +380,6 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
   uint8_t* qbuf = smem;
   uint8_t* kbuf = smem + 2 * q_bytes;
   float* aux = reinterpret_cast<float*>(kbuf + (size_t)NS * k_bytes);  // 512 floats
-  // pass-2 partial sums of the second group, 2 x 128: the upper half of aux,
-  // which pass-2 items do not use (their LSE takes at most 256 floats)
-  float* part = aux + 256;
   uint64_t* bars = reinterpret_cast<uint64_t*>(aux + 512);
   uint64_t* full = bars;
   uint64_t* empty = full + kMaxStages;
@@ -310,9 +389,7 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
   uint64_t* tempty = tfull + 2;
   uint64_t* sfull = tempty + 2;
   uint64_t* sempty = sfull + kRing;
-  uint64_t* pfull = sempty + kRing;  // part[b] written (128 arrivals)
-  uint64_t* pempty = pfull + 2;      // part[b] read (128 arrivals)
-  uint64_t* cbar = pempty + 2;       // both consumer groups (8 warp arrivals)
+  uint64_t* cbar = sempty + kRing;   // both consumer groups (8 warp arrivals)
   uint64_t* wbar = cbar + 1;         // per consumer group (4 warp arrivals each)
   uint64_t* drain = wbar + 2;        // MMA drain at teardown
   Entry* ring = reinterpret_cast<Entry*>(drain + 1);
@@ -331,8 +408,6 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       mbar_init(&qempty[b], 1);
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 8);  // the 8 consumer warps
-      mbar_init(&pfull[b], 4);  // warp arrivals
-      mbar_init(&pempty[b], 4);
       mbar_init(&wbar[b], 4);
     }
     for (int s = 0; s < kRing; ++s) {
@@ -505,7 +580,8 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
     const int lrow = quarter * 32 + lane;     // TMEM lane of this thread
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const int R = wp / 128;
-    int ring_n = 0, tile_n = 0, p2_n = 0;
+    const int half = wp >> 1;
+    int ring_n = 0, tile_n = 0;
     uint32_t cphase = 0, wphase = 0;
     // barriers over both consumer groups / this thread's group; a warp
     // arrives once its lanes' prior writes are ordered by __syncwarp
@@ -523,7 +599,10 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       wphase ^= 1;
       return r;
     };
-    float s[kTileKeys];
+    const uint64_t c2c2 = pk(c2, c2);
+    // a tile's accumulator columns of this thread: pass 1, two 32-key chunks
+    // per row block (R row blocks); pass 2, half / 32 chunks of query rows
+    uint32_t v[128];
     for (;;) {
       const int slot = ring_n % kRing;
       if (!wait_bar(&sfull[slot], (ring_n / kRing) & 1, ctl)) break;
@@ -580,10 +659,10 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       const int s_idx = e.u / p.H_kv, h = e.u % p.H_kv;
       const SeqInfo& S = p.seq[s_idx];
       bool ok = true;
-      // pass 2: this group reads the LSE of its rows [wp/2 wg, wp/2 (wg + 1));
-      // the load is issued here and lands in shared memory after the first
-      // tile's accumulator wait, which hides its latency
-      const int half = wp >> 1, li = ct & 127;
+      // pass 2: this group reads the LSE of its rows [half wg, half (wg + 1));
+      // the load is issued here and lands in shared memory (negated) after
+      // the first tile's accumulator wait, which hides its latency
+      const int li = ct & 127;
       float lv = 0.f;
       if (e.type == kP2) {
         if (!p.lse_in) {
@@ -597,10 +676,11 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
                         : __ldcg(p.lse + (size_t)e.u * wp + r);
         }
       }
-      // pass-1 running statistics of this thread's rows (R row blocks)
+      // pass-1 running reference and sum of this thread's rows (R row blocks)
       float Mrow[2] = {-INFINITY, -INFINITY}, Zrow[2] = {0.f, 0.f};
       float* raw_out = p.raw + S.score0 + (size_t)h * S.P;
       const float inv_g = 1.0f / (float)p.g;
+      const int nch = e.type == kP1 ? 2 * R : half / 32;
       for (int t = 0; t < e.ntiles; ++t, ++tile_n) {
         const int ab = tile_n & 1;  // TMEM buffer of this tile; both groups read it
         if (!wait_bar(&tfull[ab], (tile_n >> 1) & 1, ctl)) {
@@ -609,7 +689,7 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
         }
         tc_fence_after();
         if (e.type == kP2 && t == 0) {
-          if (li < half) aux[wg * half + li] = lv;
+          if (li < half) aux[wg * half + li] = -lv;
           if (!wgsync()) {
             ok = false;
             break;
@@ -617,102 +697,85 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
         }
         const int key0 = (e.tile0 + t) * kTileKeys;
         const uint32_t tb = tmem + lane_addr + (uint32_t)ab * 256u;
-        // this group's column half: keys [64 wg, 64 wg + 64) of every row
-        // block (pass 1) or query rows [wp/2 wg, wp/2 (wg + 1)) (pass 2)
+        // chunk c's first TMEM column: pass 1, row block c / 2, keys
+        // 64 wg + 32 (c % 2) of the tile; pass 2, query rows half wg + 32 c
+        const uint32_t col0 =
+            e.type == kP1 ? (uint32_t)wg * 64u : (uint32_t)(wg * half);
+        const uint32_t cstep1 = e.type == kP1 ? 32u : 32u;   // chunk 1 offset
+        const uint32_t cstep2 = e.type == kP1 ? 128u : 64u;  // chunk 2 offset
+        const uint32_t cstep3 = e.type == kP1 ? 160u : 96u;  // chunk 3 offset
+        // chunk 0 first; the others load while it is processed, and the
+        // buffer goes back to the MMA as soon as all of them have landed
         __syncwarp();  // tcgen05.ld is warp-collective
-        if (e.type == kP1) {
-          if (R == 2)
-            tmem_load64x2(tb + (uint32_t)wg * 64u, tb + 128u + (uint32_t)wg * 64u, s);
-          else
-            tmem_load64(tb + (uint32_t)wg * 64u, s);
-        } else {
-          if (wp == 256)
-            tmem_load64x2(tb + (uint32_t)wg * 128u, tb + (uint32_t)wg * 128u + 64u, s);
-          else
-            tmem_load64(tb + (uint32_t)wg * 64u, s);
+        tmem_ld32_async(tb + col0, v);
+        tmem_wait32(v);
+        tmem_ld32_async(tb + col0 + cstep1, v + 32);
+        if (nch == 4) {
+          tmem_ld32_async(tb + col0 + cstep2, v + 64);
+          tmem_ld32_async(tb + col0 + cstep3, v + 96);
         }
-        // the accumulator is in registers: hand the buffer back to the MMA
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[ab]);
         if (e.type == kP1) {
-#pragma unroll
-          for (int rb = 0; rb < 2; ++rb) {
-            if (rb >= R) break;
-            float* v = s + rb * 64;
-            const int row = rb * 128 + lrow;
-            const int limit = min(S.P + row / p.g, S.L - 1) - (key0 + wg * 64);  // last visible
-            float tmax = -INFINITY;
-            if (limit >= 63) {
-#pragma unroll
-              for (int j = 0; j < 64; ++j) tmax = fmaxf(tmax, v[j]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 64; ++j) {
-                if (j > limit) v[j] = -INFINITY;
-                tmax = fmaxf(tmax, v[j]);
+          const int lim0 = min(S.P + lrow / p.g, S.L - 1) - (key0 + wg * 64);  // row block 0
+          const int lim1 = min(S.P + (128 + lrow) / p.g, S.L - 1) - (key0 + wg * 64);
+          auto chunk = [&](uint32_t* vc, int lim, float& M, float& Z) {
+            if (M != -INFINITY && lim >= 31) {
+              const float z = p1_chunk_sum(vc, c2c2, pk(-M, -M));
+              const float Zn = Z + z;
+              if (Zn < 0x1p64f) {
+                Z = Zn;
+                return;
               }
+              // a logit far above the running reference (or an overflow):
+              // redo the chunk with an exact one (rare)
             }
-            if (tmax != -INFINITY) {  // some key of this half tile is visible to the row
-              const float Mn = fmaxf(Mrow[rb], tmax * c2);
-              float z = Zrow[rb] * ex2(Mrow[rb] - Mn);
-              float z1 = 0.f, z2 = 0.f, z3 = 0.f;
-#pragma unroll
-              for (int j = 0; j < 64; j += 4) {
-                z += ex2(fmaf(v[j], c2, -Mn));
-                z1 += ex2(fmaf(v[j + 1], c2, -Mn));
-                z2 += ex2(fmaf(v[j + 2], c2, -Mn));
-                z3 += ex2(fmaf(v[j + 3], c2, -Mn));
-              }
-              Zrow[rb] = (z + z1) + (z2 + z3);
-              Mrow[rb] = Mn;
-            }
-          }
-        } else if (PER_Q) {
-          // every query head keeps its own sum: member m of the group owns
-          // the rows r with r % g == m; the two groups' halves add up in the
-          // zeroed score array (two addends onto zero: order-independent)
-          float am[8];
-          if (wp == 256)
-            row_sum_members<128>(s, aux + wg * 128, c2, am);
-          else
-            row_sum_members<64>(s, aux + wg * 64, c2, am);
-          const int key = key0 + lrow;
-          if (key < S.P) {
-            float* base = p.raw + S.score0 + (size_t)h * p.g * S.P + key;
-            for (int m = 0; m < p.g; ++m) {
-              float v = 0.f;
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                if (k % p.g == m) v += am[k];
-              atomicAdd(base + (size_t)m * S.P, v);
-            }
+            p1_chunk_exact(vc, lim, c2, M, Z);
+          };
+          chunk(v, lim0, Mrow[0], Zrow[0]);
+          if (nch == 4) tmem_wait96(v + 32); else tmem_wait32(v + 32);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[ab]);
+          chunk(v + 32, lim0 - 32, Mrow[0], Zrow[0]);
+          if (R == 2) {
+            chunk(v + 64, lim1, Mrow[1], Zrow[1]);
+            chunk(v + 96, lim1 - 32, Mrow[1], Zrow[1]);
           }
         } else {
-          const float acc = wp == 256 ? row_sum<128>(s, aux + wg * 128, c2)
-                                      : row_sum<64>(s, aux + wg * 64, c2);
-          // combine the two halves of this key's sum in shared memory
-          const int pb = p2_n & 1;
-          const uint32_t pph = (p2_n >> 1) & 1;
-          ++p2_n;
-          if (wg == 1) {
-            if (!wait_bar(&pempty[pb], pph ^ 1, ctl)) {
-              ok = false;
-              break;
+          uint64_t acc[4] = {0, 0, 0, 0};
+          const float* nl = aux + wg * half;
+          p2_chunk(v, nl, c2c2, acc);
+          if (nch == 4) tmem_wait96(v + 32); else tmem_wait32(v + 32);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty[ab]);
+          p2_chunk(v + 32, nl + 32, c2c2, acc);
+          if (nch == 4) {
+            p2_chunk(v + 64, nl + 64, c2c2, acc);
+            p2_chunk(v + 96, nl + 96, c2c2, acc);
+          }
+          const int key = key0 + lrow;
+          if (PER_Q) {
+            // every query head keeps its own sum: member m of the group owns
+            // the rows r with r % g == m (g divides 8; acc[k] holds the
+            // columns 2k, 2k+1 mod 8); the two groups' halves add up in the
+            // zeroed score array (two addends onto zero: order-independent)
+            float am[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) upk(acc[k], am[2 * k], am[2 * k + 1]);
+            if (key < S.P) {
+              float* base = p.raw + S.score0 + (size_t)h * p.g * S.P + key;
+              for (int m = 0; m < p.g; ++m) {
+                float x = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                  if (k % p.g == m) x += am[k];
+                atomicAdd(base + (size_t)m * S.P, x);
+              }
             }
-            part[pb * 128 + lrow] = acc;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&pfull[pb]);
-          } else {
-            if (!wait_bar(&pfull[pb], pph, ctl)) {
-              ok = false;
-              break;
-            }
-            const float other = part[pb * 128 + lrow];
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&pempty[pb]);
-            const int key = key0 + lrow;
-            if (key < S.P) raw_out[key] = (acc + other) * inv_g;
+          } else if (key < S.P) {
+            // the two groups' halves meet in the zeroed score array (two
+            // addends onto zero: the result does not depend on their order)
+            atomicAdd(raw_out + key, sum4(acc) * inv_g);
           }
         }
       }
@@ -789,81 +852,21 @@ bool make_map(CUtensorMap* m, const void* base, int d, int heads, long long rows
 
 }  // namespace tc
 
-// Builds the item queue for one launch group and launches the kernel, or
-// declines (taken = false) for shapes it does not cover.
+// Builds the item queues for one launch group and launches the kernel, or
+// declines (taken = false) for shapes it does not cover: anything but bf16
+// with d in {64, 128} and W * g in {128, 256}.  A shape it covers always runs
+// here: a launch group with more KV heads than one launch's queue can describe
+// is split into several launches, and any failure is returned as an error.
 int launch_score_tc(const Plan& p, void* stream, bool* taken) {
   using namespace tc;
   *taken = false;
   if (p.dtype != 0 || (p.d != 64 && p.d != 128) || (p.Wp != 128 && p.Wp != 256)) return cudaSuccess;
-  if (p.chunk_keys != kTileKeys * kTilesPerPiece || p.counters == nullptr) return cudaSuccess;
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) return cudaErrorUnknown;
-  }
-  TcPlan tp;
-  std::memset(&tp, 0, sizeof tp);
-  tp.wp = p.Wp;
-  tp.counters = p.counters;
-  // groups of whole KV heads, ~kGroupTiles key tiles each
-  const int units = p.nseq * p.H_kv;
-  int g = 0, acc = 0, u0 = 0;
-  for (int u = 0; u < units; ++u) {
-    const SeqInfo& S = p.seq[u / p.H_kv];
-    if (S.scored) acc += (S.L + kTileKeys - 1) / kTileKeys;
-    const bool last = u == units - 1;
-    if (acc >= kGroupTiles || (last && acc > 0)) {
-      if (g == kMaxGroups) return cudaSuccess;  // too many groups: leave it to the other path
-      tp.grp[g].u0 = u0;
-      tp.grp[g].u1 = u + 1;
-      ++g;
-      u0 = u + 1;
-      acc = 0;
-    }
-  }
-  tp.ngroups = g;
-  if (g == 0) return cudaSuccess;
-  for (int i = 0; i < g; ++i) {
-    Group& G = tp.grp[i];
-    for (int u = G.u0; u < G.u1; ++u) {
-      const SeqInfo& S = p.seq[u / p.H_kv];
-      if (!S.scored) continue;
-      const int t1 = (S.L + kTileKeys - 1) / kTileKeys, t2 = (S.P + kTileKeys - 1) / kTileKeys;
-      G.p1_items += (t1 + kTilesPerPiece - 1) / kTilesPerPiece;
-      G.p2_items += (t2 + kTilesPerPiece - 1) / kTilesPerPiece;
-    }
-    G.m_items = ((G.u1 - G.u0) * p.Wp + kMergeRows - 1) / kMergeRows;
-  }
-  // queue order: P1(0) | P1(1) M(0) | P1(2) M(1) P2(0) | ... | M(G-1) P2(G-2) | P2(G-1):
-  // merges follow the next group's pass 1, pass 2 trails by two groups, so
-  // pass-2 items rarely wait for their merge while K is still in L2
-  int idx = 0;
-  if (p.lse_in) {  // the caller's LSE: pass 2 only
-    for (int k = 0; k < g; ++k) {
-      Group& G = tp.grp[k];
-      G.p1_items = G.m_items = 0;
-      G.p1_start = G.m_start = 1 << 30;
-      G.p2_start = idx;
-      idx += G.p2_items;
-    }
-  }
-  for (int k = 0; k <= g + 1 && !p.lse_in; ++k) {
-    if (k < g) {
-      tp.grp[k].p1_start = idx;
-      idx += tp.grp[k].p1_items;
-    }
-    if (k >= 1 && k - 1 < g) {
-      tp.grp[k - 1].m_start = idx;
-      idx += tp.grp[k - 1].m_items;
-    }
-    if (k >= 2) {
-      tp.grp[k - 2].p2_start = idx;
-      idx += tp.grp[k - 2].p2_items;
-    }
-  }
-  tp.total_items = idx;
+  *taken = true;
+  if (p.chunk_keys != kTileKeys * kTilesPerPiece || p.counters == nullptr)
+    return cudaErrorInvalidValue;
+  const DeviceInfo* di = current_device_info();
+  if (!di) return cudaErrorUnknown;
+  const int sms = di->sms;
 
   const uint32_t halves = p.d / 64;
   const uint32_t q_bytes = (uint32_t)p.Wp * 128u * halves;
@@ -873,25 +876,21 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken) {
   const long long room = (long long)kSmemLimit - 2 * (long long)q_bytes - misc;
   int stages = (int)(room / k_bytes);
   if (stages > 6) stages = 6;
-  if (stages < 2) return cudaSuccess;
-  tp.stages = stages;
+  if (stages < 2) return cudaErrorInvalidConfiguration;  // cannot happen for W * g <= 256
   const size_t smem = 2 * (size_t)q_bytes + (size_t)stages * k_bytes + misc;
 
-  if (p.g > 256 || p.W > 256) return cudaSuccess;
   // the K map covers the rows of the whole call (rows past the end read as zeros)
   CUtensorMap tm_k, tm_q;
-  if (!make_map(&tm_k, p.k, p.d, p.H_kv, p.total_rows, 1, kTileKeys)) return cudaSuccess;
-  if (!make_map(&tm_q, p.q, p.d, p.H_q, (long long)p.batch * p.W, p.g, p.W)) return cudaSuccess;
+  if (!make_map(&tm_k, p.k, p.d, p.H_kv, p.total_rows, 1, kTileKeys) ||
+      !make_map(&tm_q, p.q, p.d, p.H_q, (long long)p.batch * p.W, p.g, p.W))
+    return cudaErrorInvalidValue;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   auto kern = p.out_heads != p.H_kv ? score_tc_kernel<true> : score_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  // zero the queue head and the per-group counters
-  e = cudaMemsetAsync(p.counters, 0, sizeof(int) * (1 + 2 * g), st);
-  if (e != cudaSuccess) return e;
-  if (p.out_heads != p.H_kv) {  // per-query-head scores are added up by the two consumer groups
+  {  // the two consumer groups add their halves of every pass-2 sum into zeroed scores
     long long lo = -1, hi = 0;
     for (int s = 0; s < p.nseq; ++s) {
       const SeqInfo& S = p.seq[s];
@@ -904,12 +903,82 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken) {
       if (e != cudaSuccess) return e;
     }
   }
-  const int grid = sms < tp.total_items ? sms : tp.total_items;
-  kern<<<grid, kThreads, smem, st>>>(p, tp, tm_k, tm_q);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  count_launches(1);
-  *taken = true;
+
+  const int units = p.nseq * p.H_kv;
+  int u_begin = 0;
+  while (u_begin < units) {
+    TcPlan tp;
+    std::memset(&tp, 0, sizeof tp);
+    tp.wp = p.Wp;
+    tp.counters = p.counters;
+    tp.stages = stages;
+    // groups of whole KV heads, ~kGroupTiles key tiles each, at most
+    // kMaxGroups per launch
+    int g = 0, acc = 0, u0 = u_begin, u = u_begin;
+    for (; u < units && g < kMaxGroups; ++u) {
+      const SeqInfo& S = p.seq[u / p.H_kv];
+      if (S.scored) acc += (S.L + kTileKeys - 1) / kTileKeys;
+      const bool last = u == units - 1;
+      if (acc >= kGroupTiles || (last && acc > 0)) {
+        tp.grp[g].u0 = u0;
+        tp.grp[g].u1 = u + 1;
+        ++g;
+        u0 = u + 1;
+        acc = 0;
+      }
+    }
+    if (g == 0) break;  // the remaining units have nothing to score
+    u_begin = tp.grp[g - 1].u1;
+    tp.ngroups = g;
+    for (int i = 0; i < g; ++i) {
+      Group& G = tp.grp[i];
+      for (int x = G.u0; x < G.u1; ++x) {
+        const SeqInfo& S = p.seq[x / p.H_kv];
+        if (!S.scored) continue;
+        const int t1 = (S.L + kTileKeys - 1) / kTileKeys, t2 = (S.P + kTileKeys - 1) / kTileKeys;
+        G.p1_items += (t1 + kTilesPerPiece - 1) / kTilesPerPiece;
+        G.p2_items += (t2 + kTilesPerPiece - 1) / kTilesPerPiece;
+      }
+      G.m_items = ((G.u1 - G.u0) * p.Wp + kMergeRows - 1) / kMergeRows;
+    }
+    // queue order: P1(0) | P1(1) M(0) | P1(2) M(1) P2(0) | ... | M(G-1) P2(G-2) | P2(G-1):
+    // merges follow the next group's pass 1, pass 2 trails by two groups, so
+    // pass-2 items rarely wait for their merge while K is still in L2
+    int idx = 0;
+    if (p.lse_in) {  // the caller's LSE: pass 2 only
+      for (int k = 0; k < g; ++k) {
+        Group& G = tp.grp[k];
+        G.p1_items = G.m_items = 0;
+        G.p1_start = G.m_start = 1 << 30;
+        G.p2_start = idx;
+        idx += G.p2_items;
+      }
+    }
+    for (int k = 0; k <= g + 1 && !p.lse_in; ++k) {
+      if (k < g) {
+        tp.grp[k].p1_start = idx;
+        idx += tp.grp[k].p1_items;
+      }
+      if (k >= 1 && k - 1 < g) {
+        tp.grp[k - 1].m_start = idx;
+        idx += tp.grp[k - 1].m_items;
+      }
+      if (k >= 2) {
+        tp.grp[k - 2].p2_start = idx;
+        idx += tp.grp[k - 2].p2_items;
+      }
+    }
+    tp.total_items = idx;
+    // zero the queue head and the per-group counters
+    e = cudaMemsetAsync(p.counters, 0, sizeof(int) * (1 + 2 * g), st);
+    if (e != cudaSuccess) return e;
+    const int grid = sms < tp.total_items ? sms : tp.total_items;
+    kern<<<grid, kThreads, smem, st>>>(p, tp, tm_k, tm_q);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launches(1);
+    count_score_launches(kScorePathTensorCores, 1);
+  }
   return cudaSuccess;
 }
 

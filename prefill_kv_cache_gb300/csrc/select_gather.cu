@@ -30,6 +30,8 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "plan.h"
 
 namespace cg = cooperative_groups;
@@ -532,7 +534,9 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
 
 namespace {
 
-int g_max_cluster = 0;  // largest cluster size this GPU allows for the kernel (16 or 8)
+constexpr int kMaxDevices = 64;
+std::mutex g_cluster_mu;
+int g_max_cluster[kMaxDevices] = {};  // per device: largest cluster size allowed (16 or 8)
 
 size_t smem_for(int CS, int maxP, int kp) {
   const int slice = (maxP + CS - 1) / CS;
@@ -568,18 +572,24 @@ int launch_select_gather(const Plan& p, void* stream) {
   cudaError_t e = cudaFuncSetAttribute(select_gather, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kStageFloats * (int)sizeof(float));
   if (e != cudaSuccess) return e;
-  static int sms = 0;
-  if (g_max_cluster == 0) {
-    g_max_cluster = 8;
-    if (cudaFuncSetAttribute(select_gather, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-            cudaSuccess &&
-        max_active_clusters(kMaxCluster, 64 * 1024) > 0)
-      g_max_cluster = kMaxCluster;
-    cudaGetLastError();
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (sms <= 0) sms = 1;
+  const DeviceInfo* di = current_device_info();
+  int dev = 0;
+  if (!di || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return cudaErrorUnknown;
+  const int sms = di->sms;
+  int max_cluster = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_cluster_mu);
+    if (g_max_cluster[dev] == 0) {
+      int mc = 8;
+      if (cudaFuncSetAttribute(select_gather, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                               1) == cudaSuccess &&
+          max_active_clusters(kMaxCluster, 64 * 1024) > 0)
+        mc = kMaxCluster;
+      cudaGetLastError();
+      g_max_cluster[dev] = mc;
+    }
+    max_cluster = g_max_cluster[dev];
   }
   // Cluster size: a power of two, large enough that all units together fill
   // the GPU and each slice fits the shared-memory staging, then halved while
@@ -590,7 +600,7 @@ int launch_select_gather(const Plan& p, void* stream) {
     if (p.seq[s].scored) maxP = max(maxP, p.seq[s].P);
   const int room = kStageFloats - raw_span(p.kp / 2);
   int CS = 1;
-  while (CS < g_max_cluster && (units * CS < sms || (maxP + CS - 1) / CS > room)) CS *= 2;
+  while (CS < max_cluster && (units * CS < sms || (maxP + CS - 1) / CS > room)) CS *= 2;
   while (CS > 1 && (maxP + CS / 2 - 1) / (CS / 2) <= room &&
          max_active_clusters(CS, smem_for(CS, maxP, p.kp)) < units)
     CS /= 2;

@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "plan.h"
 #include "snapkv.h"
@@ -18,6 +19,35 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken);
 
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+static std::atomic<uint64_t> g_score_launches[2];
+void count_score_launches(int path, int n) {
+  g_score_launches[path].fetch_add((uint64_t)n, std::memory_order_relaxed);
+}
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+DeviceInfo g_dev_info[kMaxDevices];
+bool g_dev_known[kMaxDevices] = {};
+}  // namespace
+
+const DeviceInfo* current_device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (!g_dev_known[dev]) {
+    DeviceInfo d{};
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        d.sms <= 0 || d.smem_optin <= 0)
+      return nullptr;
+    g_dev_info[dev] = d;
+    g_dev_known[dev] = true;
+  }
+  return &g_dev_info[dev];
+}
 
 namespace {
 
@@ -318,6 +348,11 @@ int snapkv_score_with_lse(const snapkv_shape* shape, const void* q_win, const vo
 }
 
 uint64_t snapkv_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+uint64_t snapkv_score_path_launches(int32_t path) {
+  if (path != SNAPKV_SCORE_PATH_TENSOR_CORES && path != SNAPKV_SCORE_PATH_CUDA_CORES) return 0;
+  return g_score_launches[path].load(std::memory_order_relaxed);
+}
 
 int snapkv_get_status(const void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || workspace_bytes < sizeof(int)) return SNAPKV_ERR_INVALID_ARG;

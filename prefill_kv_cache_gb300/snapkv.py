@@ -41,7 +41,9 @@ EXPORTED = (
     "snapkv_host_staging_size",
     "snapkv_compress_host",
     "snapkv_compress_noalloc",
+    "snapkv_noalloc_get_status",
     "snapkv_kernel_launches",
+    "snapkv_score_path_launches",
     "snapkv_status_string",
     "snapkv_version",
 )
@@ -102,6 +104,8 @@ def load() -> ctypes.CDLL:
     lib.snapkv_compress_all_queries.restype = ctypes.c_int
     lib.snapkv_kernel_launches.argtypes = []
     lib.snapkv_kernel_launches.restype = ctypes.c_uint64
+    lib.snapkv_score_path_launches.argtypes = [i32]
+    lib.snapkv_score_path_launches.restype = ctypes.c_uint64
     lib.snapkv_score_offsets.argtypes = [shp, vp, i32, i32, ctypes.POINTER(sz),
                                          ctypes.POINTER(sz), ctypes.POINTER(sz)]
     lib.snapkv_score_offsets.restype = ctypes.c_int
@@ -115,6 +119,8 @@ def load() -> ctypes.CDLL:
     lib.snapkv_compress_noalloc.argtypes = [shp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                             vp]
     lib.snapkv_compress_noalloc.restype = ctypes.c_int
+    lib.snapkv_noalloc_get_status.argtypes = [vp]
+    lib.snapkv_noalloc_get_status.restype = ctypes.c_int
     lib.snapkv_status_string.argtypes = [ctypes.c_int]
     lib.snapkv_status_string.restype = ctypes.c_char_p
     lib.snapkv_version.argtypes = []
@@ -310,6 +316,14 @@ def kernel_launches() -> int:
     return int(load().snapkv_kernel_launches())
 
 
+SCORE_PATH_TENSOR_CORES, SCORE_PATH_CUDA_CORES = 0, 1
+
+
+def score_path_launches(path: int) -> int:
+    """snapkv_score_path_launches (include/snapkv.h)."""
+    return int(load().snapkv_score_path_launches(int(path)))
+
+
 def get_status(workspace: torch.Tensor, stream=None) -> int:
     return int(load().snapkv_get_status(workspace.data_ptr(),
                                         workspace.numel() * workspace.element_size(),
@@ -364,7 +378,21 @@ def compress_noalloc(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seql
     16 MiB scratch serves as workspace.  All buffers are the caller's.
     """
     B, W, H_q, d = q_win.shape
-    shape = make_shape(B, H_q, k.shape[1], d, q_win.dtype)
+    H_kv = k.shape[1]
+    C = int(max_capacity_prompt)
+    if W != int(window_size):
+        raise ValueError("q_win's second dimension must equal window_size")
+    for name, t in (("q_win", q_win), ("k", k), ("v", v), ("out_k", out_k), ("out_v", out_v),
+                    ("out_idx", out_idx)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    for name, t, want in (("out_k", out_k, (B, C, H_kv, d)), ("out_v", out_v, (B, C, H_kv, d)),
+                          ("out_idx", out_idx, (B, H_kv, C))):
+        if tuple(t.shape) != want:
+            raise ValueError(f"{name} must have shape {want}")
+    if out_idx.dtype != torch.int32 or out_k.dtype != k.dtype or out_v.dtype != k.dtype:
+        raise ValueError("out_idx must be int32 and out_k / out_v of k's dtype")
+    shape = make_shape(B, H_q, H_kv, d, q_win.dtype)
     arr, _ = _seqlens_array(seqlens)
     rc = load().snapkv_compress_noalloc(ctypes.byref(shape), q_win.data_ptr(), k.data_ptr(),
                                         v.data_ptr(), arr, W, int(kernel_size),
@@ -373,6 +401,12 @@ def compress_noalloc(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seql
                                         _stream_handle(stream))
     if rc:
         raise SnapKVError(rc, "snapkv_compress_noalloc")
+
+
+def noalloc_get_status(stream=None) -> int:
+    """snapkv_noalloc_get_status (include/snapkv.h): synchronize the stream and
+    read the status word of the last snapkv_compress_noalloc."""
+    return int(load().snapkv_noalloc_get_status(_stream_handle(stream)))
 
 
 # ---- decode step over a KV cache (include/snapkv.h, snapkv_decode_attention) ----

@@ -5,8 +5,9 @@ The caller's window LSE comes from tests/parity.window_lse (fp64 on the CPU,
 rounded to fp32 as a prefill kernel would return it).  With it the library
 runs only the column-sum sweep over K; the scores, the selection and the
 gathered rows must meet the same agreement rule as snapkv_compress
-(tests/parity.py).  Sequences kept whole get NaN LSE rows, which must never
-be read.
+(tests/parity.py), with the LSE-input tolerance parity.LSE_RTOL (an outside
+LSE does not cancel the fp32 rounding of a row's dominant logit).  Sequences
+kept whole get NaN LSE rows, which must never be read.
 """
 import numpy as np
 import pytest
@@ -39,46 +40,26 @@ def test_small_shapes_with_lse(case):
     launches = S.kernel_launches()
     gpu = parity.run_gpu(lay, kp, pool, C, lse=lse)
     ora = parity.oracle_for(lay, kp, pool, C)
-    parity.check(lay, gpu, ora, C)
+    parity.check(lay, gpu, ora, C, rtol=parity.LSE_RTOL)
     if any(L > C for L in seqlens):
         # one score launch (tensor cores, or the pass-2 kernel alone), one selection
         assert S.kernel_launches() - launches == 2
 
 
-@pytest.mark.parametrize("name,seqs", [("2", None), ("4", [0]), ("5a", [7, 8])])
-def test_workload_with_lse(name, seqs):
+@pytest.mark.parametrize("name", ["2", "3", "4", "5a"])
+def test_workload_with_lse(name):
+    """Every sequence and KV head of the full-size workload, LSE-input mode,
+    against the oracle."""
     cfg = synth.CONFIGS[name]
     lay = synth.make_layer(name)
     lse = parity.window_lse(lay, cfg["C"])
     gpu = parity.run_gpu(lay, cfg["k_pool"], cfg["pool"], cfg["C"], lse=lse)
-    ora = parity.oracle_for(lay, cfg["k_pool"], cfg["pool"], cfg["C"], seqs=seqs)
-    parity.check(lay, gpu, ora, cfg["C"], seqs=seqs)
+    ora = parity.oracle_for(lay, cfg["k_pool"], cfg["pool"], cfg["C"])
+    parity.check(lay, gpu, ora, cfg["C"], rtol=parity.LSE_RTOL)
     for b in range(lay.B):
         for h in range(lay.H_kv):
             kept = set(gpu["idx"][b, h].tolist())
             assert all(p in kept for p in lay.targets[b][h]), (b, h)
-
-
-def test_lse_mode_agrees_with_two_pass_mode():
-    """Same inputs through snapkv_compress and snapkv_compress_with_lse."""
-    cfg = synth.CONFIGS["3"]
-    lay = synth.make_layer("3")
-    lse = parity.window_lse(lay, cfg["C"])
-    a = parity.run_gpu(lay, cfg["k_pool"], cfg["pool"], cfg["C"])
-    b = parity.run_gpu(lay, cfg["k_pool"], cfg["pool"], cfg["C"], lse=lse)
-    np.testing.assert_allclose(b["raw"], a["raw"], rtol=2e-5, atol=1e-7)
-    np.testing.assert_allclose(b["pooled"], a["pooled"], rtol=2e-5, atol=1e-7)
-    # kept sets may differ only between scores within the tolerance of the
-    # (C-W)-th best pooled score
-    n = cfg["C"] - lay.W
-    pooled = parity.unpack_scores(a["pooled"], lay.seqlens, lay.H_kv, lay.W, cfg["C"])
-    for bi in range(lay.B):
-        for h in range(lay.H_kv):
-            po = pooled[bi][h]
-            tau = np.sort(po)[::-1][n - 1]
-            diff = set(a["idx"][bi, h, :n].tolist()) ^ set(b["idx"][bi, h, :n].tolist())
-            bad = [j for j in diff if abs(po[j] - tau) > 4e-5 * tau]
-            assert not bad, (bi, h, bad[:8])
 
 
 def test_score_with_lse_fills_raw_scores():
@@ -94,5 +75,5 @@ def test_score_with_lse_fills_raw_scores():
     raw, _ = S.scores_from_workspace(ws, shape, lay.seqlens, lay.W, C)
     ora = parity.oracle_for(lay, 1, "avg", C, seqs=[0])
     got = parity.unpack_scores(raw.cpu().numpy(), lay.seqlens, lay.H_kv, lay.W, C)
-    np.testing.assert_allclose(got[0], np.stack(ora["raw"][0]), rtol=parity.RTOL,
+    np.testing.assert_allclose(got[0], np.stack(ora["raw"][0]), rtol=parity.LSE_RTOL,
                                atol=parity.ATOL)

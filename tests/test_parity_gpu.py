@@ -3,7 +3,7 @@
 Small shapes are compared in full (several tiles, ragged tails, keep-all
 sequences mixed in, every pooling kind and size); the named workloads run at
 full size in the same launch configuration the benchmark times, and the oracle
-checks a sample of their sequences one by one.  The agreement rule is in
+checks every sequence and KV head of them.  The agreement rule is in
 tests/parity.py.
 """
 import numpy as np
@@ -79,20 +79,21 @@ def _assert_planted(lay, gpu):
             assert not missing, (b, h, missing[:8])
 
 
-@pytest.mark.parametrize("name,layer,seqs", [
-    ("3", 0, [0, 5]),
-    ("4", 0, [0]),
-    ("4", 31, [0]),
-    ("5a", 0, [7, 8]),     # the shortest and the longest prompt of the ragged batch
-    ("5b", 0, [0]),
+@pytest.mark.parametrize("name,layer", [
+    ("3", 0),      # all 8 prompts of 32768 tokens
+    ("4", 0),
+    ("4", 31),
+    ("5a", 0),     # all 16 ragged prompts
+    ("5b", 0),
 ])
-def test_workload_full_size_sampled(name, layer, seqs):
+def test_workload_full_size(name, layer):
+    """Every sequence and KV head of the full-size workload against the oracle."""
     cfg = synth.CONFIGS[name]
     lay = synth.make_layer(name, layer)
     gpu = parity.run_gpu(lay, cfg["k_pool"], cfg["pool"], cfg["C"])
     _assert_planted(lay, gpu)
-    ora = parity.oracle_for(lay, cfg["k_pool"], cfg["pool"], cfg["C"], seqs=seqs)
-    parity.check(lay, gpu, ora, cfg["C"], seqs=seqs)
+    ora = parity.oracle_for(lay, cfg["k_pool"], cfg["pool"], cfg["C"])
+    parity.check(lay, gpu, ora, cfg["C"])
 
 
 def test_repeated_calls_reuse_workspace():
@@ -154,7 +155,29 @@ def test_score_path_selection(H_q, H_kv, d, W, dtype, tc):
     shape = S.make_shape(1, H_q, H_kv, d, q.dtype)
     ws = torch.empty(S.workspace_size(shape, [3000], W, 512), dtype=torch.uint8, device="cuda")
     n0 = S.kernel_launches()
+    paths0 = [S.score_path_launches(x) for x in (S.SCORE_PATH_TENSOR_CORES,
+                                                 S.SCORE_PATH_CUDA_CORES)]
     S.score(q, k, [3000], W, 512, ws)
     torch.cuda.synchronize()
     assert S.kernel_launches() - n0 == (1 if tc else 3)
+    paths = [S.score_path_launches(x) - y for x, y in zip((S.SCORE_PATH_TENSOR_CORES,
+                                                           S.SCORE_PATH_CUDA_CORES), paths0)]
+    assert paths == ([1, 0] if tc else [0, 1])
     assert S.get_status(ws) == S.OK
+
+
+def test_many_kv_heads_stay_on_tensor_cores():
+    """136 KV heads of 131072 tokens in one launch group: more than one
+    launch's queue can describe (128 groups of whole heads), so the call is
+    split into two tensor-core launches instead of leaving the tensor cores.
+    The first and the last prompt are compared with the oracle."""
+    seqlens = [131072] * 17
+    lay = synth.make_inputs(13, seqlens, 32, 8, 64, 32, "bf16", nspans=4)
+    paths0 = [S.score_path_launches(x) for x in (S.SCORE_PATH_TENSOR_CORES,
+                                                 S.SCORE_PATH_CUDA_CORES)]
+    gpu = parity.run_gpu(lay, 7, "max", 1024)
+    paths = [S.score_path_launches(x) - y for x, y in zip((S.SCORE_PATH_TENSOR_CORES,
+                                                           S.SCORE_PATH_CUDA_CORES), paths0)]
+    assert paths == [2, 0]
+    ora = parity.oracle_for(lay, 7, "max", 1024, seqs=[0, 16])
+    parity.check(lay, gpu, ora, 1024, seqs=[0, 16])

@@ -37,7 +37,7 @@ def test_noalloc_matches_compress_on_consecutive_calls(seqlens, H_q, H_kv, d, W,
         ov = torch.full_like(ref_v, 7)
         oi = torch.full_like(ref_i, 7)
         S.compress_noalloc(q, k, v, lay.seqlens, W, kp, pool, C, ok, ov, oi)
-        torch.cuda.synchronize()
+        assert S.noalloc_get_status() == S.OK  # synchronizes the stream
         assert torch.equal(oi, ref_i)
         assert torch.equal(ok.view(torch.int16) if ok.dtype == torch.bfloat16 else ok,
                            ref_k.view(torch.int16) if ref_k.dtype == torch.bfloat16 else ref_k)
@@ -58,3 +58,19 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     bad = S.load().snapkv_compress_noalloc(ctypes.byref(shape), fake, fake, fake, sl, 0, 7,
                                            S.POOL_MAX, 1024, fake, fake, fake, None)
     assert bad == S.ERR_INVALID_ARG
+
+
+def test_noalloc_binding_checks_its_arguments():
+    """The binding refuses what the C entry point cannot see: a window size
+    that disagrees with q_win, strided views and mis-shaped outputs."""
+    lay = synth.make_inputs(41, [3000], 32, 8, 128, 32, "bf16", nspans=2)
+    q, k, v = (parity.to_device(x) for x in (lay.q_win, lay.k, lay.v))
+    ok = torch.empty((1, 1024, 8, 128), dtype=torch.bfloat16, device="cuda")
+    ov = torch.empty_like(ok)
+    oi = torch.empty((1, 8, 1024), dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        S.compress_noalloc(q, k, v, [3000], 16, 7, "max", 1024, ok, ov, oi)
+    with pytest.raises(ValueError):
+        S.compress_noalloc(q, k, v, [3000], 32, 7, "max", 1024, ok.transpose(2, 3), ov, oi)
+    with pytest.raises(ValueError):
+        S.compress_noalloc(q, k, v, [3000], 32, 7, "max", 1024, ok, ov, oi[:, :4])
