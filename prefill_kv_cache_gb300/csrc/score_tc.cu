@@ -600,9 +600,9 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       return r;
     };
     const uint64_t c2c2 = pk(c2, c2);
-    // a tile's accumulator columns of this thread: pass 1, two 32-key chunks
-    // per row block (R row blocks); pass 2, half / 32 chunks of query rows
-    uint32_t v[128];
+    // two 32-column chunks of a tile's accumulator (pass 1: 32 keys of one
+    // query row; pass 2: 32 query rows of one key)
+    uint32_t v[64];
     for (;;) {
       const int slot = ring_n % kRing;
       if (!wait_bar(&sfull[slot], (ring_n / kRing) & 1, ctl)) break;
@@ -680,7 +680,28 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       float Mrow[2] = {-INFINITY, -INFINITY}, Zrow[2] = {0.f, 0.f};
       float* raw_out = p.raw + S.score0 + (size_t)h * S.P;
       const float inv_g = 1.0f / (float)p.g;
-      const int nch = e.type == kP1 ? 2 * R : half / 32;
+      // pass 1: the last key each of this thread's rows sees, relative to
+      // the first key of this group's half of tile 0
+      const int last0 = min(S.P + lrow / p.g, S.L - 1) - wg * 64;
+      const int last1 = min(S.P + (128 + lrow) / p.g, S.L - 1) - wg * 64;
+      // first TMEM column of this thread's share: pass 1, keys 64 wg ... of
+      // row block 0 (row block 1 is 128 columns on); pass 2, query rows
+      // half wg ...
+      const uint32_t col0 = e.type == kP1 ? (uint32_t)wg * 64u : (uint32_t)(wg * half);
+      float nl01[64];  // pass 2: -lse2 of this thread's first 64 query rows, item-constant
+      auto chunk1 = [&](uint32_t* vc, int lim, float& M, float& Z) {
+        // all 32 keys visible and a finite reference: sum against it; a sum
+        // past 2^100 means a logit far above the reference (or an overflow),
+        // and the chunk is redone with an exact reference (rare)
+        if (M != -INFINITY && lim >= 31) {
+          const float Zn = Z + p1_chunk_sum(vc, c2c2, pk(-M, -M));
+          if (Zn < 0x1p100f) {
+            Z = Zn;
+            return;
+          }
+        }
+        p1_chunk_exact(vc, lim, c2, M, Z);
+      };
       for (int t = 0; t < e.ntiles; ++t, ++tile_n) {
         const int ab = tile_n & 1;  // TMEM buffer of this tile; both groups read it
         if (!wait_bar(&tfull[ab], (tile_n >> 1) & 1, ctl)) {
@@ -694,64 +715,70 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
             ok = false;
             break;
           }
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(aux + wg * half + j);
+            nl01[j] = x.x;
+            nl01[j + 1] = x.y;
+            nl01[j + 2] = x.z;
+            nl01[j + 3] = x.w;
+          }
         }
         const int key0 = (e.tile0 + t) * kTileKeys;
-        const uint32_t tb = tmem + lane_addr + (uint32_t)ab * 256u;
-        // chunk c's first TMEM column: pass 1, row block c / 2, keys
-        // 64 wg + 32 (c % 2) of the tile; pass 2, query rows half wg + 32 c
-        const uint32_t col0 =
-            e.type == kP1 ? (uint32_t)wg * 64u : (uint32_t)(wg * half);
-        const uint32_t cstep1 = e.type == kP1 ? 32u : 32u;   // chunk 1 offset
-        const uint32_t cstep2 = e.type == kP1 ? 128u : 64u;  // chunk 2 offset
-        const uint32_t cstep3 = e.type == kP1 ? 160u : 96u;  // chunk 3 offset
-        // chunk 0 first; the others load while it is processed, and the
-        // buffer goes back to the MMA as soon as all of them have landed
+        const uint32_t tb = tmem + lane_addr + (uint32_t)ab * 256u + col0;
+        // rolling pair of 32-column chunks: chunk c + 1 loads while chunk c is
+        // processed; the buffer goes back to the MMA once the last chunk has
+        // landed in registers
         __syncwarp();  // tcgen05.ld is warp-collective
-        tmem_ld32_async(tb + col0, v);
+        tmem_ld32_async(tb, v);
         tmem_wait32(v);
-        tmem_ld32_async(tb + col0 + cstep1, v + 32);
-        if (nch == 4) {
-          tmem_ld32_async(tb + col0 + cstep2, v + 64);
-          tmem_ld32_async(tb + col0 + cstep3, v + 96);
-        }
+        tmem_ld32_async(tb + 32u, v + 32);
         if (e.type == kP1) {
-          const int lim0 = min(S.P + lrow / p.g, S.L - 1) - (key0 + wg * 64);  // row block 0
-          const int lim1 = min(S.P + (128 + lrow) / p.g, S.L - 1) - (key0 + wg * 64);
-          auto chunk = [&](uint32_t* vc, int lim, float& M, float& Z) {
-            if (M != -INFINITY && lim >= 31) {
-              const float z = p1_chunk_sum(vc, c2c2, pk(-M, -M));
-              const float Zn = Z + z;
-              if (Zn < 0x1p64f) {
-                Z = Zn;
-                return;
-              }
-              // a logit far above the running reference (or an overflow):
-              // redo the chunk with an exact one (rare)
-            }
-            p1_chunk_exact(vc, lim, c2, M, Z);
-          };
-          chunk(v, lim0, Mrow[0], Zrow[0]);
-          if (nch == 4) tmem_wait96(v + 32); else tmem_wait32(v + 32);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[ab]);
-          chunk(v + 32, lim0 - 32, Mrow[0], Zrow[0]);
+          const int lim0 = last0 - key0, lim1 = last1 - key0;
+          chunk1(v, lim0, Mrow[0], Zrow[0]);
+          tmem_wait32(v + 32);
           if (R == 2) {
-            chunk(v + 64, lim1, Mrow[1], Zrow[1]);
-            chunk(v + 96, lim1 - 32, Mrow[1], Zrow[1]);
+            __syncwarp();
+            tmem_ld32_async(tb + 128u, v);
+            chunk1(v + 32, lim0 - 32, Mrow[0], Zrow[0]);
+            tmem_wait32(v);
+            __syncwarp();
+            tmem_ld32_async(tb + 160u, v + 32);
+            chunk1(v, lim1, Mrow[1], Zrow[1]);
+            tmem_wait32(v + 32);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[ab]);
+            chunk1(v + 32, lim1 - 32, Mrow[1], Zrow[1]);
+          } else {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[ab]);
+            chunk1(v + 32, lim0 - 32, Mrow[0], Zrow[0]);
           }
         } else {
           uint64_t acc[4] = {0, 0, 0, 0};
           const float* nl = aux + wg * half;
-          p2_chunk(v, nl, c2c2, acc);
-          if (nch == 4) tmem_wait96(v + 32); else tmem_wait32(v + 32);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[ab]);
-          p2_chunk(v + 32, nl + 32, c2c2, acc);
-          if (nch == 4) {
-            p2_chunk(v + 64, nl + 64, c2c2, acc);
-            p2_chunk(v + 96, nl + 96, c2c2, acc);
+          p2_chunk(v, nl01, c2c2, acc);
+          tmem_wait32(v + 32);
+          if (half == 128) {
+            __syncwarp();
+            tmem_ld32_async(tb + 64u, v);
+            p2_chunk(v + 32, nl01 + 32, c2c2, acc);
+            tmem_wait32(v);
+            __syncwarp();
+            tmem_ld32_async(tb + 96u, v + 32);
+            p2_chunk(v, nl + 64, c2c2, acc);
+            tmem_wait32(v + 32);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[ab]);
+            p2_chunk(v + 32, nl + 96, c2c2, acc);
+          } else {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[ab]);
+            p2_chunk(v + 32, nl01 + 32, c2c2, acc);
           }
           const int key = key0 + lrow;
           if (PER_Q) {
