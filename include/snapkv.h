@@ -306,7 +306,7 @@ uint64_t snapkv_score_path_launches(int32_t path);
  * which every GPU that loads the library keeps until the process exits.
  * Problems whose snapkv_workspace_size exceeds 16 MiB are rejected with
  * SNAPKV_ERR_WORKSPACE before anything is enqueued (one Llama-3-8B-shaped
- * layer of 131072 tokens needs about 10.5 MB).  The call allocates nothing.
+ * layer of 131072 tokens needs about 12.6 MB).  The call allocates nothing.
  *
  * Every call looks up the array's device address in the calling thread's
  * current CUDA context (a runtime query that allocates nothing), so a context

@@ -50,7 +50,7 @@ struct Plan {
   int32_t* out_idx;
   float* raw;        // [sum P] packed (b, h, j)
   float* pooled;     // same packing
-  float2* stats;     // [total_pieces * Wp] (running max, sum of exp) per piece and row
+  float2* stats;     // [total_pieces * 512] partial (running max, sum of exp) per piece and row
   float* lse;        // [nseq * H_kv * Wp] natural-log LSE per (sequence, head, row)
   const float* lse_in;  // caller's window LSE [B, W, H_q] (natural log), or null
   const void* q_all;     // all-query scoring: every prompt query [T, H_q, d], or null

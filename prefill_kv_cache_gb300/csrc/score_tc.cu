@@ -49,11 +49,11 @@ namespace snapkv {
 namespace tc {
 
 constexpr int kThreads = 384;  // 3 warpgroups
-constexpr int kConsumerThreads = 256;
 constexpr int kTileKeys = 128;
 constexpr int kTilesPerPiece = 8;  // 1024 keys, the piece size of the stats layout
 constexpr int kMaxStages = 8;
 constexpr int kRing = 4;
+constexpr int kPub = 4;  // pass-1 publication slots between consumers and the helper warp
 constexpr int kMaxGroups = 128;
 constexpr int kGroupTiles = 1024;
 constexpr int kMergeRows = 32;
@@ -389,10 +389,11 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
   uint64_t* tempty = tfull + 2;
   uint64_t* sfull = tempty + 2;
   uint64_t* sempty = sfull + kRing;
-  uint64_t* cbar = sempty + kRing;   // both consumer groups (8 warp arrivals)
-  uint64_t* wbar = cbar + 1;         // per consumer group (4 warp arrivals each)
-  uint64_t* drain = wbar + 2;        // MMA drain at teardown
-  Entry* ring = reinterpret_cast<Entry*>(drain + 1);
+  uint64_t* drain = sempty + kRing;  // MMA drain at teardown
+  uint64_t* pub_full = drain + 1;     // pass-1 item finished by the 8 consumer warps
+  uint64_t* pub_empty = pub_full + kPub;  // helper done with the slot
+  int* pub_grp = reinterpret_cast<int*>(pub_empty + kPub);
+  Entry* ring = reinterpret_cast<Entry*>(pub_grp + kPub);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ring + kRing);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(abort_flag) + 1);
   const Ctl ctl{abort_flag, p.status};
@@ -408,14 +409,16 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       mbar_init(&qempty[b], 1);
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 8);  // the 8 consumer warps
-      mbar_init(&wbar[b], 4);
     }
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&sfull[s], 1);
       mbar_init(&sempty[s], 9);  // MMA thread + 8 consumer warps
     }
-    mbar_init(cbar, kConsumerThreads / 32);
     mbar_init(drain, 1);
+    for (int k = 0; k < kPub; ++k) {
+      mbar_init(&pub_full[k], 8);  // the consumer warps
+      mbar_init(&pub_empty[k], 1);
+    }
     *abort_flag = (smem_addr(smem) & 1023u) != 0 ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -571,6 +574,21 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
         }
       }
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------- helper ---
+    // publishes finished pass-1 items: waits until all 8 consumer warps have
+    // written an item's statistics, then one device-scope release increment
+    // of its group's counter makes them visible to the merge items
+    if (lane == 0) {
+      for (int n = 0;; ++n) {
+        const int k = n % kPub;
+        if (!wait_bar(&pub_full[k], (n / kPub) & 1, ctl)) break;
+        const int g = pub_grp[k];
+        if (g >= 0) red_release_add(&tp.counters[1 + g], 1);
+        mbar_arrive(&pub_empty[k]);
+        if (g < 0) break;
+      }
+    }
   } else if (warp >= 4) {
     // ----------------------------------------------------- consumers ---
     asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
@@ -582,40 +600,53 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
     const int R = wp / 128;
     const int half = wp >> 1;
     int ring_n = 0, tile_n = 0;
-    uint32_t cphase = 0, wphase = 0;
-    // barriers over both consumer groups / this thread's group; a warp
-    // arrives once its lanes' prior writes are ordered by __syncwarp
-    auto csync = [&]() -> bool {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(cbar);
-      const bool r = wait_bar(cbar, cphase, ctl);
-      cphase ^= 1;
-      return r;
-    };
-    auto wgsync = [&]() -> bool {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&wbar[wg]);
-      const bool r = wait_bar(&wbar[wg], wphase, ctl);
-      wphase ^= 1;
-      return r;
-    };
     const uint64_t c2c2 = pk(c2, c2);
     // two 32-column chunks of a tile's accumulator (pass 1: 32 keys of one
     // query row; pass 2: 32 query rows of one key)
     uint32_t v[64];
+    // pass 1: this thread's query row of a tile (row block wg when there are
+    // two, else row block 0 with the group's half of the keys) and the row's
+    // window index; both are the same for every item
+    const int prow = (R == 2 ? 128 * wg : 0) + lrow;
+    const int pwin = prow / p.g;
+    const int kofs = R == 2 ? 0 : 64 * wg;  // first key of the group's share of a tile
+    const int cw = warp - 4;                // consumer warp 0..7
+    float* wlse = aux + cw * 64;            // this warp's copy of -lse2 for rows 64..127 of its share
+    // hands a finished pass-1 item (group g; -1: no more) to the helper warp,
+    // which publishes it with one device-scope release once all 8 consumer
+    // warps have written their statistics
+    int pub_n = 0;
+    auto publish = [&](int g) -> bool {
+      const int k = pub_n % kPub;
+      const bool ok = wait_bar(&pub_empty[k], ((pub_n / kPub) & 1) ^ 1, ctl);
+      ++pub_n;
+      if (!ok) return false;
+      if (lane == 0) pub_grp[k] = g;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pub_full[k]);
+      return true;
+    };
     for (;;) {
       const int slot = ring_n % kRing;
       if (!wait_bar(&sfull[slot], (ring_n / kRing) & 1, ctl)) break;
       const Entry e = ring[slot];
       ++ring_n;
-      if (e.type == kDone) break;
-      if (!csync()) break;  // previous item fully finished by both groups
+      if (e.type == kDone) {
+        publish(-1);  // the helper warp stops
+        break;
+      }
       const Group& G = tp.grp[e.g];
+      // partial statistics per piece and row: one per row block with two
+      // row blocks (a row has one owner), one per group with one
+      const int nslot = R == 2 ? 1 : 2;
       if (e.type == kMerge) {
-        if (ct == 0) wait_counter(&tp.counters[1 + e.g], G.p1_items, ctl);
-        if (!csync() || *abort_flag) break;
-        // 8 threads per row, pieces strided over them
-        const int rl = ct >> 3, sub = ct & 7;
+        // each warp merges 4 of the item's 32 rows, 8 lanes per row with the
+        // partial statistics strided over them; every lane issues its loads
+        // before it combines any of them
+        if (lane == 0) wait_counter(&tp.counters[1 + e.g], G.p1_items, ctl);
+        __syncwarp();
+        if (*abort_flag) break;
+        const int rl = cw * 4 + (lane >> 3), sub = lane & 7;
         const int gr = e.row0 + rl;
         float M = -INFINITY, Z = 0.f;
         int u = -1, r = 0;
@@ -625,15 +656,26 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
           const SeqInfo& S = p.seq[u / p.H_kv];
           if (S.scored) {
             const int h = u % p.H_kv;
-            const float2* st = p.stats + (size_t)(S.piece0 + h * S.chunks) * wp + r;
-            for (int c = sub; c < S.chunks; c += 8) {
-              const float2 v = __ldcg(st + (size_t)c * wp);
-              if (v.x == -INFINITY) continue;
-              if (v.x > M) {
-                Z = Z * exp2f(M - v.x) + v.y;
-                M = v.x;
-              } else {
-                Z += v.y * exp2f(v.x - M);
+            const int parts = nslot * S.chunks;
+            // part c = piece (c / nslot), slot (c % nslot)
+            const float2* st = p.stats + (size_t)(S.piece0 + h * S.chunks) * 512 + r;
+            for (int c0 = sub; c0 < parts; c0 += 64) {
+              float2 x[8];
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                const int c = c0 + 8 * k;
+                x[k] = c < parts ? __ldcg(st + (size_t)(c / nslot) * 512 + (size_t)(c % nslot) * wp)
+                                 : make_float2(-INFINITY, 0.f);
+              }
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (x[k].x == -INFINITY) continue;
+                if (x[k].x > M) {
+                  Z = Z * exp2f(M - x[k].x) + x[k].y;
+                  M = x[k].x;
+                } else {
+                  Z += x[k].y * exp2f(x[k].x - M);
+                }
               }
             }
           } else {
@@ -649,58 +691,83 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
           M = Mn;
         }
         if (sub == 0 && u >= 0) p.lse[(size_t)u * wp + r] = M + log2f(Z);
-        if (!csync()) break;
-        if (ct == 0) red_release_add(&tp.counters[1 + tp.ngroups + e.g], 1);
+        // the warp's writes are ordered before one release of the counter
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sempty[slot]);
+        if (lane == 0) {
+          red_release_add(&tp.counters[1 + tp.ngroups + e.g], 1);
+          mbar_arrive(&sempty[slot]);
+        }
         continue;
       }
 
       const int s_idx = e.u / p.H_kv, h = e.u % p.H_kv;
       const SeqInfo& S = p.seq[s_idx];
       bool ok = true;
-      // pass 2: this group reads the LSE of its rows [half wg, half (wg + 1));
-      // the load is issued here and lands in shared memory (negated) after
-      // the first tile's accumulator wait, which hides its latency
-      const int li = ct & 127;
-      float lv = 0.f;
+      float nl01[64];  // pass 2: -lse2 of this thread's first 64 query rows, item-constant
       if (e.type == kP2) {
-        if (!p.lse_in) {
-          if (ct == 0) wait_counter(&tp.counters[1 + tp.ngroups + e.g], G.m_items, ctl);
-          if (!csync() || *abort_flag) break;
+        // the window rows' LSE (merged above, or the caller's): this warp's
+        // lanes need the rows half wg ... half wg + half - 1, the same for
+        // every lane; the first 64 go to registers, the rest to this warp's
+        // own shared-memory copy
+        if (!p.lse_in && lane == 0)
+          wait_counter(&tp.counters[1 + tp.ngroups + e.g], G.m_items * 8, ctl);
+        __syncwarp();
+        if (*abort_flag) break;
+        const int r0 = wg * half;  // first query row of the group's share
+        if (p.lse_in) {
+          // the caller's natural-log LSE, row r = i g + member; g divides
+          // W * g, a power of two, so it is one too
+          const int lg = __ffs(p.g) - 1;
+          const float* base = p.lse_in + (size_t)S.b * p.W * p.H_q + (size_t)h * p.g;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const int rr = r0 + j;
+            nl01[j] = -__ldg(base + (size_t)(rr >> lg) * p.H_q + (rr & (p.g - 1))) * kLog2e;
+          }
+          if (half == 128) {
+            const int ra = r0 + 64 + lane, rb = r0 + 96 + lane;
+            wlse[lane] = -__ldg(base + (size_t)(ra >> lg) * p.H_q + (ra & (p.g - 1))) * kLog2e;
+            wlse[32 + lane] = -__ldg(base + (size_t)(rb >> lg) * p.H_q + (rb & (p.g - 1))) * kLog2e;
+          }
+        } else {
+          const float4* src = reinterpret_cast<const float4*>(p.lse + (size_t)e.u * wp + r0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float4 x = __ldcg(src + j);
+            nl01[4 * j] = -x.x;
+            nl01[4 * j + 1] = -x.y;
+            nl01[4 * j + 2] = -x.z;
+            nl01[4 * j + 3] = -x.w;
+          }
+          if (half == 128) {
+            wlse[lane] = -__ldcg(p.lse + (size_t)e.u * wp + r0 + 64 + lane);
+            wlse[32 + lane] = -__ldcg(p.lse + (size_t)e.u * wp + r0 + 96 + lane);
+          }
         }
-        if (li < half) {
-          const int r = wg * half + li;
-          lv = p.lse_in ? __ldg(p.lse_in + (size_t)(S.b * p.W + r / p.g) * p.H_q +
-                                (size_t)h * p.g + r % p.g) * kLog2e  // caller's, row = i g + member
-                        : __ldcg(p.lse + (size_t)e.u * wp + r);
-        }
+        __syncwarp();
       }
-      // pass-1 running reference and sum of this thread's rows (R row blocks)
-      float Mrow[2] = {-INFINITY, -INFINITY}, Zrow[2] = {0.f, 0.f};
+      float Mr = -INFINITY, Zr = 0.f;  // pass 1: running reference and sum of this thread's row
       float* raw_out = p.raw + S.score0 + (size_t)h * S.P;
       const float inv_g = 1.0f / (float)p.g;
-      // pass 1: the last key each of this thread's rows sees, relative to
-      // the first key of this group's half of tile 0
-      const int last0 = min(S.P + lrow / p.g, S.L - 1) - wg * 64;
-      const int last1 = min(S.P + (128 + lrow) / p.g, S.L - 1) - wg * 64;
-      // first TMEM column of this thread's share: pass 1, keys 64 wg ... of
-      // row block 0 (row block 1 is 128 columns on); pass 2, query rows
-      // half wg ...
-      const uint32_t col0 = e.type == kP1 ? (uint32_t)wg * 64u : (uint32_t)(wg * half);
-      float nl01[64];  // pass 2: -lse2 of this thread's first 64 query rows, item-constant
-      auto chunk1 = [&](uint32_t* vc, int lim, float& M, float& Z) {
+      // pass 1: the last key the row sees, relative to the first key of the
+      // group's share of tile 0
+      const int last = min(S.P + pwin, S.L - 1) - kofs;
+      // first TMEM column of this thread's share: pass 1, the row block's
+      // keys (128 per row block) or the group's 64 of them; pass 2, query
+      // rows half wg ...
+      const uint32_t col0 = e.type == kP1 ? (R == 2 ? 128u * wg : 64u * wg) : (uint32_t)(wg * half);
+      auto chunk1 = [&](uint32_t* vc, int lim) {
         // all 32 keys visible and a finite reference: sum against it; a sum
         // past 2^100 means a logit far above the reference (or an overflow),
         // and the chunk is redone with an exact reference (rare)
-        if (M != -INFINITY && lim >= 31) {
-          const float Zn = Z + p1_chunk_sum(vc, c2c2, pk(-M, -M));
+        if (Mr != -INFINITY && lim >= 31) {
+          const float Zn = Zr + p1_chunk_sum(vc, c2c2, pk(-Mr, -Mr));
           if (Zn < 0x1p100f) {
-            Z = Zn;
+            Zr = Zn;
             return;
           }
         }
-        p1_chunk_exact(vc, lim, c2, M, Z);
+        p1_chunk_exact(vc, lim, c2, Mr, Zr);
       };
       for (int t = 0; t < e.ntiles; ++t, ++tile_n) {
         const int ab = tile_n & 1;  // TMEM buffer of this tile; both groups read it
@@ -709,21 +776,6 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
           break;
         }
         tc_fence_after();
-        if (e.type == kP2 && t == 0) {
-          if (li < half) aux[wg * half + li] = -lv;
-          if (!wgsync()) {
-            ok = false;
-            break;
-          }
-#pragma unroll
-          for (int j = 0; j < 64; j += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(aux + wg * half + j);
-            nl01[j] = x.x;
-            nl01[j + 1] = x.y;
-            nl01[j + 2] = x.z;
-            nl01[j + 3] = x.w;
-          }
-        }
         const int key0 = (e.tile0 + t) * kTileKeys;
         const uint32_t tb = tmem + lane_addr + (uint32_t)ab * 256u + col0;
         // rolling pair of 32-column chunks: chunk c + 1 loads while chunk c is
@@ -734,31 +786,30 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
         tmem_wait32(v);
         tmem_ld32_async(tb + 32u, v + 32);
         if (e.type == kP1) {
-          const int lim0 = last0 - key0, lim1 = last1 - key0;
-          chunk1(v, lim0, Mrow[0], Zrow[0]);
+          const int lim = last - key0;
+          chunk1(v, lim);
           tmem_wait32(v + 32);
           if (R == 2) {
             __syncwarp();
-            tmem_ld32_async(tb + 128u, v);
-            chunk1(v + 32, lim0 - 32, Mrow[0], Zrow[0]);
+            tmem_ld32_async(tb + 64u, v);
+            chunk1(v + 32, lim - 32);
             tmem_wait32(v);
             __syncwarp();
-            tmem_ld32_async(tb + 160u, v + 32);
-            chunk1(v, lim1, Mrow[1], Zrow[1]);
+            tmem_ld32_async(tb + 96u, v + 32);
+            chunk1(v, lim - 64);
             tmem_wait32(v + 32);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ab]);
-            chunk1(v + 32, lim1 - 32, Mrow[1], Zrow[1]);
+            chunk1(v + 32, lim - 96);
           } else {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ab]);
-            chunk1(v + 32, lim0 - 32, Mrow[0], Zrow[0]);
+            chunk1(v + 32, lim - 32);
           }
         } else {
           uint64_t acc[4] = {0, 0, 0, 0};
-          const float* nl = aux + wg * half;
           p2_chunk(v, nl01, c2c2, acc);
           tmem_wait32(v + 32);
           if (half == 128) {
@@ -768,12 +819,12 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
             tmem_wait32(v);
             __syncwarp();
             tmem_ld32_async(tb + 96u, v + 32);
-            p2_chunk(v, nl + 64, c2c2, acc);
+            p2_chunk(v, wlse, c2c2, acc);
             tmem_wait32(v + 32);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ab]);
-            p2_chunk(v + 32, nl + 96, c2c2, acc);
+            p2_chunk(v + 32, wlse + 32, c2c2, acc);
           } else {
             tc_fence_before();
             __syncwarp();
@@ -808,29 +859,14 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       }
       if (!ok) break;
       if (e.type == kP1) {
-        // merge the two groups' statistics of each row, then publish
-        float2* comb = reinterpret_cast<float2*>(aux);
-        if (wg == 1) {
-#pragma unroll
-          for (int rb = 0; rb < 2; ++rb)
-            if (rb < R) comb[rb * 128 + lrow] = make_float2(Mrow[rb], Zrow[rb]);
-        }
-        if (!csync()) break;
-        if (wg == 0) {
-          const size_t piece = (size_t)S.piece0 + (size_t)h * S.chunks + e.piece;
-#pragma unroll
-          for (int rb = 0; rb < 2; ++rb) {
-            if (rb >= R) break;
-            const float2 o = comb[rb * 128 + lrow];
-            float M = Mrow[rb], Z = Zrow[rb];
-            const float Mn = fmaxf(M, o.x);
-            if (Mn != -INFINITY) Z = Z * ex2(M - Mn) + o.y * ex2(o.x - Mn);
-            p.stats[piece * wp + rb * 128 + lrow] = make_float2(Mn, Z);
-          }
-          // the group's writes are ordered before one release of the counter
-          if (!wgsync()) break;
-          if (ct == 0) red_release_add(&tp.counters[1 + e.g], 1);
-        }
+        // publish this row's statistics for the piece (slot wg with one row
+        // block, where the two groups hold halves of the keys); the
+        // device-scope release that publishes them takes a while (it waits
+        // for this warp's writes to land): the helper warp does it
+        const size_t piece = (size_t)S.piece0 + (size_t)h * S.chunks + e.piece;
+        const int q = R == 2 ? 0 : wg;
+        p.stats[piece * 512 + (size_t)q * wp + prow] = make_float2(Mr, Zr);
+        if (!publish(e.g)) break;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[slot]);
@@ -898,8 +934,8 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken) {
   const uint32_t halves = p.d / 64;
   const uint32_t q_bytes = (uint32_t)p.Wp * 128u * halves;
   const uint32_t k_bytes = (uint32_t)kTileKeys * 128u * halves;
-  const uint32_t misc =
-      512 * 4 + (2 * kMaxStages + 8 + 2 * kRing + 4 + 2 + 2) * 8 + kRing * sizeof(Entry) + 8;
+  const uint32_t misc = 512 * 4 + (2 * kMaxStages + 8 + 2 * kRing + 1 + 2 * kPub) * 8 +
+                        kPub * 4 + kRing * sizeof(Entry) + 8;
   const long long room = (long long)kSmemLimit - 2 * (long long)q_bytes - misc;
   int stages = (int)(room / k_bytes);
   if (stages > 6) stages = 6;

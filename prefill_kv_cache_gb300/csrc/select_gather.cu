@@ -32,6 +32,7 @@
 
 #include <mutex>
 
+#include "pdl.cuh"
 #include "plan.h"
 
 namespace cg = cooperative_groups;
@@ -131,6 +132,44 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
   __syncthreads();
   *total = tot;
   return before + x - v;
+}
+
+// Exclusive block scans of two values at once; returns a's prefix, writes
+// b's prefix and both totals.
+__device__ __forceinline__ int block_excl_scan2(int a, int b, int* wsum, int* a_total,
+                                                int* b_excl, int* b_total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = a, y = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int xa = __shfl_up_sync(0xffffffffu, x, o);
+    const int ya = __shfl_up_sync(0xffffffffu, y, o);
+    if (lane >= o) {
+      x += xa;
+      y += ya;
+    }
+  }
+  if (lane == 31) {
+    wsum[warp] = x;
+    wsum[kWarps + warp] = y;
+  }
+  __syncthreads();
+  int xb = 0, yb = 0, xt = 0, yt = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const int sx = wsum[w], sy = wsum[kWarps + w];
+    if (w < warp) {
+      xb += sx;
+      yb += sy;
+    }
+    xt += sx;
+    yt += sy;
+  }
+  __syncthreads();
+  *a_total = xt;
+  *b_total = yt;
+  *b_excl = yb + y - b;
+  return xb + x - a;
 }
 
 // Copy `cnt` rows: source position pos[i] of the sequence (KV head sh) ->
@@ -257,16 +296,21 @@ __device__ bool bulk_copy_rows(const Plan& p, const SeqInfo& S, int sh, int oh, 
 __global__ void __launch_bounds__(kSelectThreads, 2)
 select_gather(const __grid_constant__ Plan p, int cap_floats) {
   extern __shared__ __align__(16) float dyn[];  // [raw staging tile + halo][pooled slice]
-  __shared__ unsigned hist[2048];                // this CTA's digit histogram
-  __shared__ unsigned mrg[2048];                 // cluster sums of the bins this CTA owns
-  __shared__ unsigned merged[2048];              // cluster sums of all bins
-  __shared__ int wsum[kWarps];
+  // cluster-wide digit histograms, one per radix digit: CTA r holds bins
+  // [r * own, (r + 1) * own) of each, and every CTA adds its values' counts
+  // into the owners' bins through distributed shared memory
+  __shared__ unsigned hb[3][2048];
+  __shared__ unsigned hl[2048];  // this CTA's counts of the current digit, then all bins
+  __shared__ int wsum[2 * kWarps];
   __shared__ int sel_pos[kChunk];
   __shared__ int sh_digit, sh_above;
-  __shared__ int sh_cnt[2];
+  __shared__ int cl_cnt[2 * kMaxCluster];        // (above, equal) per CTA, on rank 0
   __shared__ __align__(8) uint64_t bulk_bar;
 
   cg::cluster_group cluster = cg::this_cluster();
+  // launched as a programmatic dependent of the score kernel: everything
+  // below reads what that kernel wrote
+  pdl_wait();
   const int rank = (int)cluster.block_rank();
   const int CS = (int)cluster.num_blocks();
   const int t = threadIdx.x;
@@ -309,6 +353,10 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
   }
 
   const int P = S.P, n = p.n, r = p.kp / 2;
+  // the digit histograms start at zero in every CTA before any CTA adds to
+  // them: zero, arrive on the cluster barrier now, wait after pooling
+  for (int b = t; b < 3 * 2048; b += blockDim.x) (&hb[0][0])[b] = 0u;
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   const int Sz = (P + CS - 1) / CS;
   const int j0 = min(P, rank * Sz), j1 = min(P, j0 + Sz);
   const int cnt = j1 - j0;
@@ -368,31 +416,56 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
   __syncthreads();
   const float* vals = in_smem ? spool : pooled + j0;  // this CTA's pooled slice
 
+  // the cluster barrier armed before pooling: every CTA's histograms are zero
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  const int lane = t & 31;
+  // positions per thread for the counting and compaction passes: an odd
+  // stride, so that the threads of a warp reading their i-th positions hit
+  // 32 different shared-memory banks
+  const int per = ((cnt + (int)blockDim.x - 1) / (int)blockDim.x) | 1;
+  const int xa = min(cnt, t * per), xb = min(cnt, xa + per);      // this thread's range
+  int out_before = 0, eq_before = 0, need = n, my_gt = 0, my_eq = 0;
+  int excl_gt = 0, excl_eq = 0;
+  unsigned T = 0;
   if (n > 0) {
-    // 2. radix select of the n-th largest value (digits of 11, 11 and 10 bits)
+    // 2. radix select of the n-th largest value (digits of 11, 11 and 10
+    //    bits of the fp32 pattern), one cluster barrier per digit
     unsigned prefix = 0, mask = 0;
-    int need = n;
-    int my_gt = 0, my_eq = 0;  // this CTA's values above / equal to the threshold
     for (int pass = 0; pass < 3; ++pass) {
       const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
       const int nb = pass == 2 ? 1024 : 2048;
-      const int own = nb / CS;  // bins reduced by each CTA
-      for (int b = t; b < 2048; b += blockDim.x) hist[b] = 0;
+      const int own = nb / CS;  // bins held by each CTA
+      unsigned* hd = hb[pass];
+      for (int b = t; b < nb; b += blockDim.x) hl[b] = 0u;
       __syncthreads();
-      for (int x = t; x < cnt; x += blockDim.x) {
-        const unsigned u = __float_as_uint(vals[x]);
-        if ((u & mask) == prefix) atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
+      // this CTA's counts: most lanes of a warp share one bin (scores bunch
+      // in a few exponents), so lane 0 keeps a running count of its warp's
+      // lanes in lane 0's bin and adds it only when that bin changes; the
+      // other lanes add one each
+      int run_bin = -1;
+      unsigned run_cnt = 0;
+      for (int x0 = 0; x0 < cnt; x0 += blockDim.x) {
+        const int x = x0 + t;
+        const unsigned u = x < cnt ? __float_as_uint(vals[x]) : 0u;
+        const int bin = (x < cnt && (u & mask) == prefix) ? (int)((u >> shift) & (nb - 1)) : -1;
+        const int b0 = __shfl_sync(0xffffffffu, bin, 0);
+        const unsigned same = __ballot_sync(0xffffffffu, bin == b0);
+        if (lane == 0 && b0 >= 0) {
+          if (b0 != run_bin) {
+            if (run_bin >= 0) atomicAdd(&hl[run_bin], run_cnt);
+            run_bin = b0;
+            run_cnt = 0;
+          }
+          run_cnt += (unsigned)__popc(same);
+        }
+        if (bin >= 0 && bin != b0) atomicAdd(&hl[bin], 1u);
       }
-      cluster.sync();
-      for (int b = rank * own + t; b < (rank + 1) * own; b += blockDim.x) {
-        unsigned part[kMaxCluster];  // independent remote loads
-#pragma unroll
-        for (int q = 0; q < kMaxCluster; ++q)
-          part[q] = q < CS ? cluster.map_shared_rank(hist, q)[b] : 0u;
-        unsigned sum = 0;
-#pragma unroll
-        for (int q = 0; q < kMaxCluster; ++q) sum += part[q];
-        mrg[b] = sum;
+      if (lane == 0 && run_bin >= 0) atomicAdd(&hl[run_bin], run_cnt);
+      __syncthreads();
+      // its non-empty bins go to their owners
+      for (int b = t; b < nb; b += blockDim.x) {
+        const unsigned c = hl[b];
+        if (c) atomicAdd(cluster.map_shared_rank(hd, b / own) + b, c);
       }
       cluster.sync();
       for (int b1 = t; b1 < nb; b1 += 4 * blockDim.x) {
@@ -400,11 +473,11 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int b = b1 + u * blockDim.x;
-          m4[u] = b < nb ? cluster.map_shared_rank(mrg, b / own)[b] : 0u;
+          m4[u] = b < nb ? cluster.map_shared_rank(hd, b / own)[b] : 0u;
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          if (b1 + u * blockDim.x < nb) merged[b1 + u * blockDim.x] = m4[u];
+          if (b1 + u * blockDim.x < nb) hl[b1 + u * blockDim.x] = m4[u];
       }
       __syncthreads();
       // digit D with count(> D) < need <= count(>= D); bins scanned from the top
@@ -412,7 +485,7 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int rb = 4 * t + q;
-        local[q] = rb < nb ? (int)merged[nb - 1 - rb] : 0;
+        local[q] = rb < nb ? (int)hl[nb - 1 - rb] : 0;
         lsum += local[q];
       }
       int total;
@@ -430,32 +503,33 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
         }
       }
       __syncthreads();
-      // this CTA's own values in bins above the chosen digit are above T;
-      // after the last digit, its values in that bin equal T
-      const int D = sh_digit;
-      int la = 0;
-      for (int b = D + 1 + t; b < nb; b += blockDim.x) la += (int)hist[b];
-      int la_tot;
-      block_excl_scan(la, wsum, &la_tot);
-      my_gt += la_tot;
-      if (pass == 2) my_eq = (int)hist[D];
       need -= sh_above;
-      prefix |= (unsigned)D << shift;
+      prefix |= (unsigned)sh_digit << shift;
       mask |= (unsigned)(nb - 1) << shift;
-      __syncthreads();
     }
-    const unsigned T = prefix;
+    T = prefix;
 
-    // 3. per-CTA counts above / equal to T, exchanged across the cluster
+    // 3. this CTA's values above / equal to T, per thread over its range of
+    //    consecutive positions, then across the CTA and the cluster
+    int gt = 0, eq = 0;
+    for (int x = xa; x < xb; ++x) {
+      const unsigned u = __float_as_uint(vals[x]);
+      gt += u > T;
+      eq += u == T;
+    }
+    excl_gt = block_excl_scan2(gt, eq, wsum, &my_gt, &excl_eq, &my_eq);
     if (t == 0) {
-      sh_cnt[0] = my_gt;
-      sh_cnt[1] = my_eq;
+      int* dst = cluster.map_shared_rank(cl_cnt, 0);
+      dst[2 * rank] = my_gt;
+      dst[2 * rank + 1] = my_eq;
     }
     cluster.sync();
-    int eq_before = 0, out_before = 0, eq_acc = 0;
+    // every CTA's pair, fetched in parallel (one remote load per thread)
+    if (t < 2 * CS) wsum[t] = cluster.map_shared_rank(cl_cnt, 0)[t];
+    __syncthreads();
+    int eq_acc = 0;
     for (int q = 0; q < CS; ++q) {
-      const int* rc = cluster.map_shared_rank(sh_cnt, q);
-      const int g_ = rc[0], e_ = rc[1];
+      const int g_ = wsum[2 * q], e_ = wsum[2 * q + 1];
       const int take = min(max(need - eq_acc, 0), e_);
       if (q < rank) {
         out_before += g_ + take;
@@ -463,45 +537,20 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
       }
       eq_acc += e_;
     }
-    cluster.sync();  // nobody leaves while others still read its shared memory
 
-    // 4. ascending compaction of the slice into the index output, kPer
-    //    consecutive positions per thread per pass
-    int running = 0;
-    for (int base = 0; base < cnt; base += kChunk) {
-      const int x0 = base + t * kPer;
-      bool gt[kPer], eq[kPer];
-      int n_eq = 0;
-#pragma unroll
-      for (int q = 0; q < kPer; ++q) {
-        const bool in = x0 + q < cnt;
-        const unsigned u = in ? __float_as_uint(vals[x0 + q]) : 0u;
-        gt[q] = in && u > T;
-        eq[q] = in && u == T;
-        n_eq += eq[q];
+    // 4. ascending compaction: a thread's kept positions go to consecutive
+    //    slots after those of lower threads and lower CTAs; equal values are
+    //    kept in position order while the cluster still needs them
+    int slot = out_before + excl_gt + min(max(need - eq_before, 0), excl_eq);
+    int eq_rank = eq_before + excl_eq;
+    for (int x = xa; x < xb; ++x) {
+      const unsigned u = __float_as_uint(vals[x]);
+      const bool keep = u > T || (u == T && eq_rank < need);
+      eq_rank += u == T;
+      if (keep) {
+        if (slot < n) idx_out[slot] = j0 + x;  // slots from n on belong to the window
+        ++slot;
       }
-      int chunk_eq, chunk_sel;
-      int eq_rank = eq_before + block_excl_scan(n_eq, wsum, &chunk_eq);
-      bool sel[kPer];
-      int n_sel = 0;
-#pragma unroll
-      for (int q = 0; q < kPer; ++q) {
-        sel[q] = gt[q] || (eq[q] && eq_rank < need);
-        eq_rank += eq[q];
-        n_sel += sel[q];
-      }
-      int pos = block_excl_scan(n_sel, wsum, &chunk_sel);
-      // slots past n would belong to the window block: never written from here
-      const int room = max(0, min(chunk_sel, n - (out_before + running)));
-#pragma unroll
-      for (int q = 0; q < kPer; ++q) {
-        if (sel[q]) {
-          if (pos < room) idx_out[out_before + running + pos] = j0 + x0 + q;
-          ++pos;
-        }
-      }
-      eq_before += chunk_eq;
-      running += chunk_sel;
     }
   }
 
@@ -607,17 +656,20 @@ int launch_select_gather(const Plan& p, void* stream) {
   const size_t smem = smem_for(CS, maxP, p.kp);
   const int cap_floats = (int)(smem / sizeof(float));
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = CS;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: scheduled while the score kernel drains
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3(CS, units);
   cfg.blockDim = dim3(kSelectThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, select_gather, p, cap_floats);
   if (e != cudaSuccess) return e;
   count_launches(1);

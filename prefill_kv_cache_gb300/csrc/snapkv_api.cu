@@ -121,8 +121,11 @@ Layout layout_for(const snapkv_shape* sh, const int32_t* seqlens, int W, int C,
   off = align_up(off + scores * sizeof(float));
   lay.pooled = off;
   off = align_up(off + scores * sizeof(float));
+  // 512 partial (max, sum) statistics per piece: the tensor-core kernel's
+  // consumer groups publish theirs separately (2 per row at W * g = 256, 4 at
+  // 128); the CUDA-core kernels use one per row (W * g <= 256 of them)
   lay.stats = off;
-  off = align_up(off + max_pieces * Wp * sizeof(float2));
+  off = align_up(off + max_pieces * 512 * sizeof(float2));
   lay.lse = off;
   off = align_up(off + max_units * Wp * sizeof(float));
   lay.score_count = scores;
