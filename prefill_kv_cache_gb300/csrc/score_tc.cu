@@ -39,6 +39,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 
 #include "plan.h"
@@ -49,6 +50,7 @@ namespace snapkv {
 namespace tc {
 
 constexpr int kThreads = 384;  // 3 warpgroups
+constexpr int kConsumerThreads = 256;
 constexpr int kTileKeys = 128;
 constexpr int kTilesPerPiece = 8;  // 1024 keys, the piece size of the stats layout
 constexpr int kMaxStages = 8;
@@ -56,6 +58,7 @@ constexpr int kRing = 4;
 constexpr int kPub = 4;  // pass-1 publication slots between consumers and the helper warp
 constexpr int kMaxGroups = 128;
 constexpr int kGroupTiles = 1024;
+constexpr int kMinGroups = 8;  // groups per launch the sizing aims for
 constexpr int kMergeRows = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSmemLimit = 232448;
@@ -859,6 +862,17 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       }
       if (!ok) break;
       if (e.type == kP1) {
+        // clear the piece's prefix keys in the score array, into which pass 2
+        // adds its two halves; the release below orders these stores before
+        // every pass-2 item of the group
+        {
+          const int k_lo = e.tile0 * kTileKeys;
+          const int k_hi = min(S.P, k_lo + e.ntiles * kTileKeys);
+          const int rows = PER_Q ? p.g : 1;  // score vectors per KV head
+          float* z = p.raw + S.score0 + (size_t)h * rows * S.P;
+          for (int m = 0; m < rows; ++m)
+            for (int k = k_lo + ct; k < k_hi; k += kConsumerThreads) z[(size_t)m * S.P + k] = 0.f;
+        }
         // publish this row's statistics for the piece (slot wg with one row
         // block, where the two groups hold halves of the keys); the
         // device-scope release that publishes them takes a while (it waits
@@ -920,7 +934,7 @@ bool make_map(CUtensorMap* m, const void* base, int d, int heads, long long rows
 // with d in {64, 128} and W * g in {128, 256}.  A shape it covers always runs
 // here: a launch group with more KV heads than one launch's queue can describe
 // is split into several launches, and any failure is returned as an error.
-int launch_score_tc(const Plan& p, void* stream, bool* taken) {
+int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) {
   using namespace tc;
   *taken = false;
   if (p.dtype != 0 || (p.d != 64 && p.d != 128) || (p.Wp != 128 && p.Wp != 256)) return cudaSuccess;
@@ -953,7 +967,7 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  {  // the two consumer groups add their halves of every pass-2 sum into zeroed scores
+  if (p.lse_in) {  // no pass 1 to clear the scores: pass 2 adds two halves into zeroed ones
     long long lo = -1, hi = 0;
     for (int s = 0; s < p.nseq; ++s) {
       const SeqInfo& S = p.seq[s];
@@ -968,6 +982,16 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken) {
   }
 
   const int units = p.nseq * p.H_kv;
+  // groups of whole KV heads of about group_tiles key tiles: at most
+  // kGroupTiles, and small enough that a launch has several groups, so that
+  // pass 2 of one group overlaps pass 1 of the next ones
+  long long total_tiles = 0;
+  for (int u = 0; u < units; ++u) {
+    const SeqInfo& S = p.seq[u / p.H_kv];
+    if (S.scored) total_tiles += (S.L + kTileKeys - 1) / kTileKeys;
+  }
+  const int group_tiles =
+      (int)std::max(1LL, std::min((long long)kGroupTiles, total_tiles / kMinGroups));
   int u_begin = 0;
   while (u_begin < units) {
     TcPlan tp;
@@ -982,7 +1006,7 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken) {
       const SeqInfo& S = p.seq[u / p.H_kv];
       if (S.scored) acc += (S.L + kTileKeys - 1) / kTileKeys;
       const bool last = u == units - 1;
-      if (acc >= kGroupTiles || (last && acc > 0)) {
+      if (acc >= group_tiles || (last && acc > 0)) {
         tp.grp[g].u0 = u0;
         tp.grp[g].u1 = u + 1;
         ++g;
@@ -1032,9 +1056,16 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken) {
       }
     }
     tp.total_items = idx;
-    // zero the queue head and the per-group counters
-    e = cudaMemsetAsync(p.counters, 0, sizeof(int) * (1 + 2 * g), st);
-    if (e != cudaSuccess) return e;
+    // the queue head and the per-group counters: a fresh slice of the
+    // call's zeroed counter region (zeroed again when it runs out)
+    const int need = 1 + 2 * g;
+    if (*counter_off + need > kCounterInts) {
+      e = cudaMemsetAsync(p.counters, 0, sizeof(int) * kCounterInts, st);
+      if (e != cudaSuccess) return e;
+      *counter_off = 0;
+    }
+    tp.counters = p.counters + *counter_off;
+    *counter_off += need;
     const int grid = sms < tp.total_items ? sms : tp.total_items;
     kern<<<grid, kThreads, smem, st>>>(p, tp, tm_k, tm_q);
     e = cudaGetLastError();

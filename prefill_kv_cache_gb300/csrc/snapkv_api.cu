@@ -15,7 +15,8 @@
 
 namespace snapkv {
 
-int launch_score_tc(const Plan& p, void* stream, bool* taken);
+// counter_off: next unused int of the call's zeroed counter region (in/out)
+int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off);
 
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
@@ -217,7 +218,13 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
 
   char* ws = static_cast<char*>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ws + lay.status, 0, sizeof(int), st) != cudaSuccess) return SNAPKV_ERR_CUDA;
+  // one memset per call: the status word and the work-queue counters, which
+  // sit together at the start of the workspace
+  static_assert(sizeof(int) * kCounterInts % 4 == 0, "counter region");
+  if (cudaMemsetAsync(ws + lay.status, 0, lay.counters + sizeof(int) * kCounterInts - lay.status,
+                      st) != cudaSuccess)
+    return SNAPKV_ERR_CUDA;
+  int counter_off = 0;
 
   const int H = shape->num_kv_heads;
   Plan p;
@@ -282,7 +289,7 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
       if (launch_score_allq(p, stream) != cudaSuccess) return SNAPKV_ERR_CUDA;
     } else if (piece > 0) {
       bool taken = false;
-      if (launch_score_tc(p, stream, &taken) != cudaSuccess) return SNAPKV_ERR_CUDA;
+      if (launch_score_tc(p, stream, &taken, &counter_off) != cudaSuccess) return SNAPKV_ERR_CUDA;
       if (!taken && launch_score_simt(p, stream) != cudaSuccess) return SNAPKV_ERR_CUDA;
     }
     if (!score_only && launch_select_gather(p, stream) != cudaSuccess) return SNAPKV_ERR_CUDA;
