@@ -55,6 +55,7 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-scissorhands", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true")
     ap.add_argument("--case", choices=["decode", "scissorhands"], default=None,
                     help="run a small fixed case for a profiler and exit (no timing)")
     return ap.parse_args()
@@ -174,29 +175,165 @@ def compute_peaks(sms: int):
     return tc, tc_kind, mufu, f"derived: {MUFU_EX2_PER_CLK_SM} ex2/clk/SM x {sms} SMs x {mhz:.0f} MHz"
 
 
-def cpu_baseline(name, layers_total, nthreads=None, lay=None, min_seconds=10.0, max_layers=4):
+def cpu_baseline(name, layers_total, nthreads=None, lay=None, min_seconds=10.0, max_layers=4,
+                 keep_first=False):
     """Oracle on whole layers (all KV heads), layer 0 onwards, until about
-    min_seconds of CPU time are spent (at most max_layers): a bounded sample."""
+    min_seconds of CPU time are spent (at most max_layers): a bounded sample.
+    The oracle uses all host cores: (sequence, KV head) units in parallel, or
+    one unit at a time with its window rows and keys spread over the cores
+    when there are fewer units than cores.  keep_first: also return layer 0
+    and the oracle's outputs for it (the bench's parity check)."""
     import oracle
     import synth
 
     cfg = synth.CONFIGS[name]
+    nthreads = nthreads or (os.cpu_count() or 1)
     dt, tokens, done = 0.0, 0, 0
+    first = None
     while done < max_layers and (done == 0 or dt < min_seconds):
         cur = lay if (lay is not None and done == 0) else synth.make_layer(name, done)
-        units = cur.B * cur.H_kv
-        nthreads = nthreads or max(1, min(units, os.cpu_count() or 1))
         t0 = time.perf_counter()
-        oracle.compress(cur.q_win, cur.k, cur.v, cur.seqlens, cur.W, cfg["k_pool"], cfg["pool"],
-                        cfg["C"], nthreads=nthreads)
+        out = oracle.compress(cur.q_win, cur.k, cur.v, cur.seqlens, cur.W, cfg["k_pool"],
+                              cfg["pool"], cfg["C"], nthreads=nthreads)
         dt += time.perf_counter() - t0
+        if keep_first and done == 0:
+            first = (cur, out)
         tokens += int(sum(cur.seqlens))
         done += 1
         if lay is not None:
             break
-    return {"value": tokens / dt, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+    info = {"value": tokens / dt, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "host_cores": os.cpu_count(), "threads": nthreads,
             "sample": f"layers 0-{done - 1} of {layers_total}, all KV heads, "
-                      f"{tokens} prompt tokens, fp64 C oracle, {dt:.2f} s"}
+                      f"{tokens} prompt tokens, fp64 C oracle on {nthreads} threads, {dt:.2f} s"}
+    return (info, first) if keep_first else info
+
+
+def single_thread_baseline(name="2"):
+    """The oracle on one thread over one layer of a workload (tokens/s)."""
+    import oracle
+    import synth
+
+    cfg = synth.CONFIGS[name]
+    lay = synth.make_layer(name, 0)
+    t0 = time.perf_counter()
+    oracle.compress(lay.q_win, lay.k, lay.v, lay.seqlens, lay.W, cfg["k_pool"], cfg["pool"],
+                    cfg["C"], nthreads=1)
+    return int(sum(lay.seqlens)) / (time.perf_counter() - t0)
+
+
+def parity_vs_oracle(S, torch, lay, ora, cfg, dev):
+    """The library's compression of one numpy layer against the oracle's, by
+    the agreement rule of the parity tests: raw and pooled scores within
+    1e-7 + 1e-5 |oracle|; kept prefix sets equal outside the band of pooled
+    scores within 1e-5 relative of the (C - W)-th best; every slot holds the
+    bytes of its own index's K and V rows; the window block is exact."""
+    import numpy as np
+
+    def to_dev(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return (t.view(torch.bfloat16) if a.dtype == np.uint16 else t).to(dev)
+
+    W, C, H_kv = lay.W, cfg["C"], lay.H_kv
+    q, k, v = to_dev(lay.q_win), to_dev(lay.k), to_dev(lay.v)
+    ok, ov, oi, ws = S.compress(q, k, v, lay.seqlens, W, cfg["k_pool"], cfg["pool"], C)
+    shape = S.make_shape(lay.B, lay.H_q, H_kv, lay.d, q.dtype)
+    raw, pooled = S.scores_from_workspace(ws, shape, lay.seqlens, W, C)
+    torch.cuda.synchronize()
+    raw, pooled = raw.cpu().numpy(), pooled.cpu().numpy()
+    idx = oi.cpu().numpy()
+    bits = lambda t: t.cpu().view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 \
+        else t.cpu().numpy()
+    okh, ovh = bits(ok), bits(ov)
+    n = C - W
+    off, units, band, decided, worst, ok_all = 0, 0, 0, 0, 0.0, True
+    for b, L in enumerate(lay.seqlens):
+        L = int(L)
+        P = L - W
+        for h in range(H_kv):
+            gi = idx[b, h]
+            if L > C:
+                units += 1
+                for got, want in ((raw[off + h * P: off + (h + 1) * P], ora["raw"][b][h]),
+                                  (pooled[off + h * P: off + (h + 1) * P], ora["pooled"][b][h])):
+                    err = np.abs(got - want)
+                    ok_all &= bool(np.all(err <= 1e-7 + 1e-5 * np.abs(want)))
+                    worst = max(worst, float(np.max(err / (1e-7 + 1e-5 * np.abs(want)))))
+                po, tau = ora["pooled"][b][h], ora["tau"][b, h]
+                band += int(np.count_nonzero(np.abs(po - tau) <= 1e-5 * tau))
+                diff = set(gi[:n].tolist()) ^ set(ora["idx"][b, h, :n].tolist())
+                decided += len(diff)
+                ok_all &= all(abs(po[j] - tau) <= 1e-5 * tau for j in diff)
+                ok_all &= gi[n:].tolist() == list(range(P, L))
+            else:
+                ok_all &= gi.tolist() == ora["idx"][b, h].tolist()
+            rows = gi >= 0
+            src = lay.offsets[b] + gi[rows]
+            ok_all &= bool(np.array_equal(okh[b, rows, h], lay.k[src, h]))
+            ok_all &= bool(np.array_equal(ovh[b, rows, h], lay.v[src, h]))
+        if L > C:
+            off += H_kv * P
+    return {"layer": 0, "units": units, "pass": bool(ok_all),
+            "max_score_error_over_tolerance": worst,
+            "exemption_band_positions": band, "kept_by_one_side_in_band": decided,
+            "rule": "scores 1e-7 + 1e-5 rel; sets equal outside the 1e-5 band; bytes by index"}
+
+
+def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=10):
+    """Every other workload of the pages' shapes through snapkv_compress (and
+    snapkv_score alone), four layers in rotation so that inputs exceed L2:
+    microseconds per layer, prompt tokens/s and the fraction of the HBM
+    roofline of the algorithmic bytes."""
+    import synth
+    from synth.device import make_layer_device
+
+    out = {}
+    for name in names:
+        cfg = synth.CONFIGS[name]
+        W, C, kp, pool = cfg["W"], cfg["C"], cfg["k_pool"], cfg["pool"]
+        layers = [make_layer_device(name, l, dev) for l in range(4)]
+        seqlens = layers[0][3]
+        B, H_q, H_kv, d = len(seqlens), cfg["H_q"], cfg["H_kv"], cfg["d"]
+        dt = layers[0][1].dtype
+        esz = 2 if cfg["dtype"] == "bf16" else 4
+        shape = S.make_shape(B, H_q, H_kv, d, dt)
+        ws = torch.empty(S.workspace_size(shape, seqlens, W, C), dtype=torch.uint8, device=dev)
+        ok = torch.empty((B, C, H_kv, d), dtype=dt, device=dev)
+        ov, oi = torch.empty_like(ok), torch.empty((B, H_kv, C), dtype=torch.int32, device=dev)
+
+        def comp(i):
+            q, k, v, _ = layers[i % 4]
+            S.compress(q, k, v, seqlens, W, kp, pool, C, out_k=ok, out_v=ov, out_idx=oi,
+                       workspace=ws)
+
+        def score(i):
+            q, k, _, _ = layers[i % 4]
+            S.score(q, k, seqlens, W, C, ws)
+
+        res = {"desc": cfg["desc"]}
+        for tag, fn in (("compress", comp), ("score", score)):
+            for i in range(4):
+                fn(i)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for i in range(reps):
+                fn(i)
+            b.record()
+            torch.cuda.synchronize()
+            res[f"us_per_layer_{tag}"] = 1e3 * a.elapsed_time(b) / reps
+        assert S.get_status(ws) == S.OK
+        score_bytes, compress_bytes = workload_bytes(cfg, seqlens, esz)
+        us = res["us_per_layer_compress"]
+        res["tokens_per_s"] = sum(seqlens) / (us / 1e6)
+        res["frac_compress"] = compress_bytes / (us / 1e6) / 1e9 / peak
+        res["frac_score"] = score_bytes / (res["us_per_layer_score"] / 1e6) / 1e9 / peak
+        res["bytes_per_layer"] = compress_bytes
+        out[name] = res
+        del layers
+    out["note"] = ("four layers in rotation, CUDA events around 10 calls; fractions of the "
+                   "measured HBM copy bandwidth for the algorithmic bytes")
+    return out
 
 
 def run_reference(args, rank, world):
@@ -226,6 +363,7 @@ def run_reference(args, rank, world):
                    else len(seqlens), "layers": layers,
                    "step": "oracle on a bounded sample: one full layer, all KV heads"},
         "cpu_baseline": {"kind": "oracle", "cores": vals[0]["cores"],
+                         "host_cores": vals[0]["host_cores"], "threads": vals[0]["threads"],
                          "sample": vals[0]["sample"], "value": v, "unit": UNIT},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -360,9 +498,15 @@ def main():
     if not args.no_e2e:
         e2e = run_e2e(S, torch, data, seqlens, cfg, shape, dev, stream, args, layers)
 
-    cpu = None
+    workloads = None
+    if rank == 0 and name == "4" and not args.no_workloads:
+        workloads = workload_table(S, torch, dev, peak)
+
+    cpu, parity = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(name, layers)
+        cpu, (lay0, ora0) = cpu_baseline(name, layers, keep_first=True)
+        cpu["single_thread_cfg2_tokens_per_s"] = single_thread_baseline("2")
+        parity = parity_vs_oracle(S, torch, lay0, ora0, cfg, dev)
 
     if rank == 0:
         clk = sampler.summary()
@@ -397,6 +541,8 @@ def main():
                 "frac": exps / (score_avg_ms / 1e3) / 1e12 / mufu_peak,
                 "exp2_per_launch": exps, "peak_kind": mufu_kind},
             "cpu_baseline": cpu,
+            "parity": parity,
+            "workloads": workloads,
             "e2e": e2e,
             "decode": decode,
             "scissorhands": sh_decode,

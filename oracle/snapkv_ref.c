@@ -126,6 +126,134 @@ int ref_scores_unit(const void *q_win, const void *k, int dtype, int W, int H_q,
 }
 
 /*
+ * ref_scores_unit with its window rows spread over nthreads POSIX threads,
+ * giving the same doubles bit for bit: each row's logits, maximum, sum and
+ * probabilities are computed by the same expressions in the same order as
+ * there, and kept; the per-key sums then add the rows in the same order
+ * (query head major, window row minor), starting from zero, and the window
+ * mass adds the same terms in the same order.  Only the work is split.
+ */
+typedef struct {
+    const void *q_win, *k;
+    int dtype, W, H_q, H_kv, d, b, h, L, P, g;
+    long long off;
+    double *prob;  /* [W*g][P]   probabilities of the prefix keys per row */
+    double *win;   /* [W*g][W]   probabilities of the window keys per row */
+    double *raw;
+    int nthreads, status;
+} ref_rows_job;
+
+typedef struct {
+    ref_rows_job *job;
+    int tid;
+} ref_rows_arg;
+
+static void *ref_rows_worker(void *p)
+{
+    ref_rows_arg *a = (ref_rows_arg *)p;
+    ref_rows_job *J = a->job;
+    int W = J->W, d = J->d, P = J->P, g = J->g;
+    double *s = (double *)malloc(sizeof(double) * (size_t)J->L);
+    if (!s) {
+        J->status = REF_ERR_NOMEM;
+        return NULL;
+    }
+    for (int row = a->tid; row < W * g; row += J->nthreads) {
+        int r = row / W, i = row % W; /* rows ordered query head major */
+        int hq = J->h * g + r;
+        int t = P + i;
+        size_t qbase = (((size_t)J->b * W + i) * J->H_q + hq) * (size_t)d;
+        double m = -INFINITY, Z = 0.0;
+        for (int j = 0; j <= t; j++) {
+            size_t kbase = (((size_t)(J->off + j)) * J->H_kv + J->h) * (size_t)d;
+            double dot = 0.0;
+            for (int c = 0; c < d; c++)
+                dot += ref_elem(J->q_win, J->dtype, qbase + c) * ref_elem(J->k, J->dtype, kbase + c);
+            s[j] = dot / sqrt((double)d);
+            if (!isfinite(s[j])) {
+                J->status = REF_ERR_NONFINITE;
+                free(s);
+                return NULL;
+            }
+            if (s[j] > m)
+                m = s[j];
+        }
+        for (int j = 0; j <= t; j++)
+            Z += exp(s[j] - m);
+        for (int j = 0; j < P; j++)
+            J->prob[(size_t)row * P + j] = exp(s[j] - m) / Z;
+        for (int j = P; j <= t; j++)
+            J->win[(size_t)row * W + (j - P)] = exp(s[j] - m) / Z;
+    }
+    free(s);
+    return NULL;
+}
+
+static void *ref_keys_worker(void *p)
+{
+    ref_rows_arg *a = (ref_rows_arg *)p;
+    ref_rows_job *J = a->job;
+    int rows = J->W * J->g, P = J->P;
+    int per = (P + J->nthreads - 1) / J->nthreads;
+    int j0 = a->tid * per, j1 = j0 + per < P ? j0 + per : P;
+    for (int j = j0; j < j1; j++) {
+        double acc = 0.0;
+        for (int row = 0; row < rows; row++)
+            acc += J->prob[(size_t)row * P + j];
+        J->raw[j] = acc / (double)J->g;
+    }
+    return NULL;
+}
+
+int ref_scores_unit_mt(const void *q_win, const void *k, int dtype, int W, int H_q, int H_kv,
+                       int d, int b, int h, int L, long long off, double *raw,
+                       double *window_mass, int nthreads)
+{
+    ref_rows_job J;
+    pthread_t th[256];
+    ref_rows_arg args[256];
+    int P = L - W;
+    if (nthreads <= 1)
+        return ref_scores_unit(q_win, k, dtype, W, H_q, H_kv, d, b, h, L, off, raw, window_mass);
+    if (P < 1 || H_kv < 1 || H_q % H_kv != 0 || d < 1)
+        return REF_ERR_ARG;
+    if (nthreads > 256)
+        nthreads = 256;
+    memset(&J, 0, sizeof J);
+    J.q_win = q_win; J.k = k; J.dtype = dtype; J.W = W; J.H_q = H_q; J.H_kv = H_kv;
+    J.d = d; J.b = b; J.h = h; J.L = L; J.P = P; J.g = H_q / H_kv; J.off = off;
+    J.raw = raw; J.nthreads = nthreads;
+    J.prob = (double *)malloc(sizeof(double) * (size_t)W * J.g * (size_t)P);
+    J.win = (double *)malloc(sizeof(double) * (size_t)W * J.g * (size_t)W);
+    if (!J.prob || !J.win) { /* not enough memory to keep the rows: one thread */
+        free(J.prob);
+        free(J.win);
+        return ref_scores_unit(q_win, k, dtype, W, H_q, H_kv, d, b, h, L, off, raw, window_mass);
+    }
+    for (int t = 0; t < nthreads; t++) {
+        args[t].job = &J;
+        args[t].tid = t;
+        pthread_create(&th[t], NULL, ref_rows_worker, &args[t]);
+    }
+    for (int t = 0; t < nthreads; t++)
+        pthread_join(th[t], NULL);
+    if (!J.status) {
+        double wm = 0.0;
+        for (int t = 0; t < nthreads; t++)
+            pthread_create(&th[t], NULL, ref_keys_worker, &args[t]);
+        for (int t = 0; t < nthreads; t++)
+            pthread_join(th[t], NULL);
+        for (int row = 0; row < W * J.g; row++)
+            for (int i = 0; i < (row % W) + 1; i++)
+                wm += J.win[(size_t)row * W + i];
+        *window_mass = wm / (double)J.g;
+    }
+    free(J.prob);
+    free(J.win);
+    return J.status;
+}
+
+/*
  * Step 3: 1-D pooling of raw[0..P) with kernel kp (odd), stride 1 and kp/2
  * zeros of padding on each side.  Average: window sum / kp (the zeros count,
  * at the edges too).  Maximum: largest value in the zero-padded window.
@@ -209,6 +337,7 @@ typedef struct {
     void *out_k, *out_v;
     int *out_idx;
     int nthreads;
+    int inner;  /* threads per unit's scores (units run one at a time when > 1) */
     int status;
     pthread_mutex_t lock;
 } ref_job;
@@ -230,9 +359,9 @@ static int ref_compress_unit(ref_job *J, int b, int h)
         J->tau[(size_t)b * J->H_kv + h] = NAN;
         if (P >= 1) {
             /* scores are still defined and reported */
-            rc = ref_scores_unit(J->q_win, J->k, J->dtype, W, J->H_q, J->H_kv, d, b, h,
-                                 L, J->offs[b], J->raw + so,
-                                 J->window_mass + (size_t)b * J->H_kv + h);
+            rc = ref_scores_unit_mt(J->q_win, J->k, J->dtype, W, J->H_q, J->H_kv, d, b, h,
+                                    L, J->offs[b], J->raw + so,
+                                    J->window_mass + (size_t)b * J->H_kv + h, J->inner);
             if (rc)
                 return rc;
             rc = ref_pool(J->raw + so, P, J->kp, J->pool_type, J->pooled + so);
@@ -241,9 +370,9 @@ static int ref_compress_unit(ref_job *J, int b, int h)
         }
     } else {
         double tau;
-        rc = ref_scores_unit(J->q_win, J->k, J->dtype, W, J->H_q, J->H_kv, d, b, h, L,
-                             J->offs[b], J->raw + so,
-                             J->window_mass + (size_t)b * J->H_kv + h);
+        rc = ref_scores_unit_mt(J->q_win, J->k, J->dtype, W, J->H_q, J->H_kv, d, b, h, L,
+                                J->offs[b], J->raw + so,
+                                J->window_mass + (size_t)b * J->H_kv + h, J->inner);
         if (rc)
             return rc;
         rc = ref_pool(J->raw + so, P, J->kp, J->pool_type, J->pooled + so);
@@ -321,6 +450,11 @@ int ref_compress(const void *q_win, const void *k, const void *v, int dtype, int
     J.seqlens = seqlens; J.offs = offs; J.score_offs = score_offs;
     J.raw = raw; J.pooled = pooled; J.tau = tau; J.window_mass = window_mass;
     J.out_k = out_k; J.out_v = out_v; J.out_idx = out_idx; J.nthreads = nthreads;
+    J.inner = 1;
+    if (B * H_kv < nthreads) { /* fewer units than threads: one unit at a time, all threads on it */
+        J.inner = nthreads;
+        J.nthreads = nthreads = 1;
+    }
     pthread_mutex_init(&J.lock, NULL);
     th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)nthreads);
     args = (ref_worker_arg *)malloc(sizeof(ref_worker_arg) * (size_t)nthreads);

@@ -374,3 +374,18 @@ def test_per_q_head_scores_average_to_the_group_score():
     for hq in range(8):
         rows = b["idx"][0, hq]
         np.testing.assert_array_equal(b["out_k"][0, :, hq], lay.k[rows, hq // g])
+
+
+def test_oracle_threaded_scores_are_bit_identical():
+    """With fewer (sequence, KV head) units than threads the oracle spreads
+    one unit's window rows and keys over the threads; the doubles must not
+    change (same expressions, same summation order)."""
+    lay = synth.make_inputs(61, [700, 530], 8, 2, 64, 16, "fp32", nspans=2)
+    a = oracle.compress(lay.q_win, lay.k, lay.v, lay.seqlens, 16, 5, "avg", 128, nthreads=1)
+    b = oracle.compress(lay.q_win, lay.k, lay.v, lay.seqlens, 16, 5, "avg", 128, nthreads=7)
+    for x, y in zip(a["raw"], b["raw"]):
+        assert np.array_equal(x, y)
+    for x, y in zip(a["pooled"], b["pooled"]):
+        assert np.array_equal(x, y)
+    assert np.array_equal(a["window_mass"], b["window_mass"])
+    assert np.array_equal(a["idx"], b["idx"])
