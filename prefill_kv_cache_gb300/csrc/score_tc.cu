@@ -52,7 +52,7 @@ namespace tc {
 constexpr int kThreads = 384;  // 3 warpgroups
 constexpr int kConsumerThreads = 256;
 constexpr int kTileKeys = 128;
-constexpr int kTilesPerPiece = 8;  // 1024 keys, the piece size of the stats layout
+constexpr int kTilesPerPiece = 8;  // at most 1024 keys per piece (the call chooses)
 constexpr int kMaxStages = 8;
 constexpr int kRing = 4;
 constexpr int kPub = 4;  // pass-1 publication slots between consumers and the helper warp
@@ -74,6 +74,7 @@ struct Group {
 
 struct TcPlan {
   int ngroups, total_items, stages, wp;
+  int tpp;        // key tiles per piece (the call's piece size / 128)
   int* counters;  // [0] queue head; [1+g] pass-1 pieces done; [1+G+g] merges done
   Group grp[kMaxGroups];
 };
@@ -348,12 +349,12 @@ __device__ Entry decode(const Plan& p, const TcPlan& tp, int idx) {
       if (!S.scored) continue;
       const int keys = kind == kP1 ? S.L : S.P;
       const int tiles = ceil_div(keys, kTileKeys);
-      const int pieces = ceil_div(tiles, kTilesPerPiece);
+      const int pieces = ceil_div(tiles, tp.tpp);
       if (local < pieces) {
         e.u = u;
         e.piece = local;
-        e.tile0 = local * kTilesPerPiece;
-        e.ntiles = min(kTilesPerPiece, tiles - e.tile0);
+        e.tile0 = local * tp.tpp;
+        e.ntiles = min(tp.tpp, tiles - e.tile0);
         return e;
       }
       local -= pieces;
@@ -939,8 +940,10 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) 
   *taken = false;
   if (p.dtype != 0 || (p.d != 64 && p.d != 128) || (p.Wp != 128 && p.Wp != 256)) return cudaSuccess;
   *taken = true;
-  if (p.chunk_keys != kTileKeys * kTilesPerPiece || p.counters == nullptr)
+  if (p.chunk_keys % kTileKeys != 0 || p.chunk_keys > kTileKeys * kTilesPerPiece ||
+      p.counters == nullptr)
     return cudaErrorInvalidValue;
+  const int tpp = p.chunk_keys / kTileKeys;
   const DeviceInfo* di = current_device_info();
   if (!di) return cudaErrorUnknown;
   const int sms = di->sms;
@@ -997,6 +1000,7 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) 
     TcPlan tp;
     std::memset(&tp, 0, sizeof tp);
     tp.wp = p.Wp;
+    tp.tpp = tpp;
     tp.counters = p.counters;
     tp.stages = stages;
     // groups of whole KV heads, ~kGroupTiles key tiles each, at most
@@ -1023,8 +1027,8 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) 
         const SeqInfo& S = p.seq[x / p.H_kv];
         if (!S.scored) continue;
         const int t1 = (S.L + kTileKeys - 1) / kTileKeys, t2 = (S.P + kTileKeys - 1) / kTileKeys;
-        G.p1_items += (t1 + kTilesPerPiece - 1) / kTilesPerPiece;
-        G.p2_items += (t2 + kTilesPerPiece - 1) / kTilesPerPiece;
+        G.p1_items += (t1 + tpp - 1) / tpp;
+        G.p2_items += (t2 + tpp - 1) / tpp;
       }
       G.m_items = ((G.u1 - G.u0) * p.Wp + kMergeRows - 1) / kMergeRows;
     }

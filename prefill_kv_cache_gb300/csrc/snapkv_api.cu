@@ -53,7 +53,9 @@ const DeviceInfo* current_device_info() {
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr int kChunkKeys = 1024;  // keys per score piece
+constexpr int kChunkKeys = 1024;    // keys per score piece, at most
+constexpr int kMinChunkKeys = 256;  // and at least
+constexpr int kTargetPieces = 4 * 152;  // pieces per pass a call aims for
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -93,7 +95,28 @@ int check_flags(const snapkv_shape* sh, int32_t flags) {
   return SNAPKV_OK;
 }
 
-int chunks_for(int L) { return (L + kChunkKeys - 1) / kChunkKeys; }
+// Keys per score piece (the unit of work of both scoring paths): 1024 for
+// the tensor-core kernel; for the CUDA-core kernels, whose blocks each take
+// one piece, less when the call has too few pieces to give every SM of a
+// GB300 (152) several of them, so that short prompts still spread over the
+// GPU.  A function of the problem only, so that the workspace size and the
+// launch agree.
+int chunk_keys_for(const snapkv_shape* sh, const int32_t* seqlens, int W, int C) {
+  int ck = kChunkKeys;
+  const int Wp = W * (sh->num_q_heads / sh->num_kv_heads);
+  if (sh->dtype == SNAPKV_BF16 && (sh->head_dim == 64 || sh->head_dim == 128) &&
+      (Wp == 128 || Wp == 256))
+    return ck;
+  for (; ck > kMinChunkKeys; ck /= 2) {
+    long long pieces = 0;
+    for (int b = 0; b < sh->batch; ++b)
+      if (seqlens[b] > C) pieces += (long long)sh->num_kv_heads * ((seqlens[b] + ck - 1) / ck);
+    if (pieces >= kTargetPieces) break;
+  }
+  return ck;
+}
+
+int chunks_for(int L, int ck) { return (L + ck - 1) / ck; }
 
 Layout layout_for(const snapkv_shape* sh, const int32_t* seqlens, int W, int C,
                   bool per_q = false) {
@@ -101,13 +124,14 @@ Layout layout_for(const snapkv_shape* sh, const int32_t* seqlens, int W, int C,
   const int H = sh->num_kv_heads;
   const int Wp = W * (sh->num_q_heads / H);
   size_t scores = 0, max_pieces = 0, max_units = 0;
+  const int ck = chunk_keys_for(sh, seqlens, W, C);
   for (int g0 = 0; g0 < sh->batch; g0 += kGroupSeqs) {
     const int g1 = std::min(sh->batch, g0 + kGroupSeqs);
     size_t pieces = 0;
     for (int b = g0; b < g1; ++b) {
       if (seqlens[b] > C) {
         scores += (size_t)(per_q ? sh->num_q_heads : H) * (seqlens[b] - W);
-        pieces += (size_t)H * chunks_for(seqlens[b]);
+        pieces += (size_t)H * chunks_for(seqlens[b], ck);
       }
     }
     max_pieces = std::max(max_pieces, pieces);
@@ -242,7 +266,7 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
   p.dtype = shape->dtype;
   p.scale = (float)(1.0 / std::sqrt((double)p.d));
   p.log2e_scale = (float)(1.4426950408889634 / std::sqrt((double)p.d));
-  p.chunk_keys = kChunkKeys;
+  p.chunk_keys = chunk_keys_for(shape, seqlens_host, W, C);
   p.q = q_win;
   p.k = k;
   p.v = v;
@@ -279,7 +303,7 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
       S.row0 = row0;
       S.score0 = score0;
       S.piece0 = piece;
-      S.chunks = S.scored ? chunks_for(S.L) : 0;
+      S.chunks = S.scored ? chunks_for(S.L, p.chunk_keys) : 0;
       piece += S.chunks * H;
       if (S.scored) score0 += (long long)p.out_heads * S.P;
       row0 += S.L;
