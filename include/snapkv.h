@@ -273,6 +273,39 @@ int snapkv_compress_host(const snapkv_shape *shape, const void *q_win_host,
                          void *stream);
 
 /*
+ * Several layers through host buffers, with the host-to-device copies of one
+ * layer overlapping the compression of the previous one.  Equivalent to
+ * snapkv_compress_host on each layer in turn (same outputs, bit for bit), but
+ * the inputs of layer l + 1 upload on `copy_stream` while layer l compresses
+ * on `stream`, through two staging slots; the call waits for both streams
+ * once, after the last layer.
+ *
+ *   n_layers     >= 1
+ *   q_win_host, k_host, v_host          arrays of n_layers host pointers, each
+ *                                        a layer's input as in snapkv_compress_host
+ *                                        (page-locked v is read in place)
+ *   out_k_host, out_v_host, out_idx_host arrays of n_layers host pointers
+ *   staging      device, 256-byte aligned, >= snapkv_host_staging_size_layers
+ *   stream, copy_stream  two different cudaStream_t of the current device
+ *   events       array of 4 cudaEvent_t created by the caller (the library
+ *                creates none); recorded and waited on by the call
+ * Returns SNAPKV_OK when every layer's outputs are complete, or the error of
+ * the first layer that failed (earlier layers' outputs may then have been
+ * written); argument errors return before anything is enqueued.
+ */
+size_t snapkv_host_staging_size_layers(const snapkv_shape *shape, const int32_t *seqlens_host,
+                                       int32_t W, int32_t C);
+
+int snapkv_compress_host_layers(const snapkv_shape *shape, int32_t n_layers,
+                                const void *const *q_win_host, const void *const *k_host,
+                                const void *const *v_host, const int32_t *seqlens_host,
+                                int32_t W, int32_t kernel_size, int32_t pool_type, int32_t C,
+                                void *const *out_k_host, void *const *out_v_host,
+                                int32_t *const *out_idx_host, void *staging,
+                                size_t staging_bytes, void *stream, void *copy_stream,
+                                void *const *events);
+
+/*
  * Number of CUDA kernels this library has launched in this process so far
  * (all devices, all streams), for launch accounting.
  */

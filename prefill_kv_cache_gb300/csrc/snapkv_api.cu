@@ -478,4 +478,77 @@ int snapkv_compress_host(const snapkv_shape* shape, const void* q_win_host, cons
   return SNAPKV_OK;
 }
 
+size_t snapkv_host_staging_size_layers(const snapkv_shape* shape, const int32_t* seqlens_host,
+                                       int32_t W, int32_t C) {
+  if (check_problem(shape, seqlens_host, W, C) != SNAPKV_OK) return 0;
+  return 2 * align_up(host_layout(shape, seqlens_host, W, C).total);
+}
+
+int snapkv_compress_host_layers(const snapkv_shape* shape, int32_t n_layers,
+                                const void* const* q_win_host, const void* const* k_host,
+                                const void* const* v_host, const int32_t* seqlens_host, int32_t W,
+                                int32_t kernel_size, int32_t pool_type, int32_t C,
+                                void* const* out_k_host, void* const* out_v_host,
+                                int32_t* const* out_idx_host, void* staging, size_t staging_bytes,
+                                void* stream, void* copy_stream, void* const* events) {
+  int rc = check_problem(shape, seqlens_host, W, C);
+  if (rc != SNAPKV_OK) return rc;
+  if (n_layers < 1 || !q_win_host || !k_host || !v_host || !out_k_host || !out_v_host ||
+      !out_idx_host || !staging || !aligned(staging, kAlign) || !events)
+    return SNAPKV_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l)
+    if (!q_win_host[l] || !k_host[l] || !v_host[l] || !out_k_host[l] || !out_v_host[l] ||
+        !out_idx_host[l])
+      return SNAPKV_ERR_INVALID_ARG;
+  for (int e = 0; e < 4; ++e)
+    if (!events[e]) return SNAPKV_ERR_INVALID_ARG;
+  const HostLayout h = host_layout(shape, seqlens_host, W, C);
+  const size_t slot = align_up(h.total);
+  if (staging_bytes < 2 * slot) return SNAPKV_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t cs = static_cast<cudaStream_t>(copy_stream);
+  cudaEvent_t uploaded[2] = {static_cast<cudaEvent_t>(events[0]),
+                             static_cast<cudaEvent_t>(events[1])};
+  cudaEvent_t done[2] = {static_cast<cudaEvent_t>(events[2]), static_cast<cudaEvent_t>(events[3])};
+  // two staging slots: layer l + 1's inputs upload on the copy stream while
+  // layer l compresses on the compute stream; a slot is refilled only after
+  // the compression that read it and the copy of its outputs have finished
+  for (int l = 0; l < n_layers; ++l) {
+    const int sl = l & 1;
+    char* base = static_cast<char*>(staging) + sl * slot;
+    const void* v_dev = base + h.v;
+    bool v_zero_copy = false;
+    {
+      cudaPointerAttributes at{};
+      if (cudaPointerGetAttributes(&at, v_host[l]) == cudaSuccess &&
+          at.type == cudaMemoryTypeHost && at.devicePointer != nullptr &&
+          aligned(at.devicePointer, 16)) {
+        v_dev = at.devicePointer;
+        v_zero_copy = true;
+      }
+      cudaGetLastError();  // a pageable pointer is not an error here
+    }
+    if (l >= 2 && cudaStreamWaitEvent(cs, done[sl], 0) != cudaSuccess) return SNAPKV_ERR_CUDA;
+    if (cudaMemcpyAsync(base + h.q, q_win_host[l], h.q_bytes, cudaMemcpyHostToDevice, cs) ||
+        cudaMemcpyAsync(base + h.k, k_host[l], h.kv_bytes, cudaMemcpyHostToDevice, cs) ||
+        (!v_zero_copy &&
+         cudaMemcpyAsync(base + h.v, v_host[l], h.kv_bytes, cudaMemcpyHostToDevice, cs)) ||
+        cudaEventRecord(uploaded[sl], cs) || cudaStreamWaitEvent(st, uploaded[sl], 0))
+      return SNAPKV_ERR_CUDA;
+    rc = enqueue(shape, base + h.q, base + h.k, v_dev, seqlens_host, W, kernel_size, pool_type,
+                 C, base + h.ok, base + h.ov, reinterpret_cast<int32_t*>(base + h.oi),
+                 base + h.ws, h.ws_bytes, stream, false, nullptr, false, nullptr, nullptr,
+                 v_zero_copy);
+    if (rc != SNAPKV_OK) return rc;
+    if (cudaMemcpyAsync(out_k_host[l], base + h.ok, h.out_bytes, cudaMemcpyDeviceToHost, st) ||
+        cudaMemcpyAsync(out_v_host[l], base + h.ov, h.out_bytes, cudaMemcpyDeviceToHost, st) ||
+        cudaMemcpyAsync(out_idx_host[l], base + h.oi, h.idx_bytes, cudaMemcpyDeviceToHost, st) ||
+        cudaEventRecord(done[sl], st))
+      return SNAPKV_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(st) != cudaSuccess || cudaStreamSynchronize(cs) != cudaSuccess)
+    return SNAPKV_ERR_CUDA;
+  return SNAPKV_OK;
+}
+
 }  // extern "C"

@@ -40,6 +40,8 @@ EXPORTED = (
     "snapkv_get_status",
     "snapkv_host_staging_size",
     "snapkv_compress_host",
+    "snapkv_host_staging_size_layers",
+    "snapkv_compress_host_layers",
     "snapkv_compress_noalloc",
     "snapkv_noalloc_get_status",
     "snapkv_kernel_launches",
@@ -116,6 +118,11 @@ def load() -> ctypes.CDLL:
     lib.snapkv_compress_host.argtypes = [shp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                          vp, sz, vp]
     lib.snapkv_compress_host.restype = ctypes.c_int
+    lib.snapkv_host_staging_size_layers.argtypes = [shp, vp, i32, i32]
+    lib.snapkv_host_staging_size_layers.restype = sz
+    lib.snapkv_compress_host_layers.argtypes = [shp, i32, vp, vp, vp, vp, i32, i32, i32, i32,
+                                                vp, vp, vp, vp, sz, vp, vp, vp]
+    lib.snapkv_compress_host_layers.restype = ctypes.c_int
     lib.snapkv_compress_noalloc.argtypes = [shp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                             vp]
     lib.snapkv_compress_noalloc.restype = ctypes.c_int
@@ -366,6 +373,46 @@ def compress_host(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seqlens
                                      _stream_handle(stream))
     if rc:
         raise SnapKVError(rc, "snapkv_compress_host")
+
+
+def host_staging_size_layers(shape: snapkv_shape, seqlens, window_size: int,
+                             max_capacity_prompt: int) -> int:
+    arr, _ = _seqlens_array(seqlens)
+    return int(load().snapkv_host_staging_size_layers(ctypes.byref(shape), arr,
+                                                      int(window_size),
+                                                      int(max_capacity_prompt)))
+
+
+def compress_host_layers(layers, seqlens, window_size: int, kernel_size: int, pooling,
+                         max_capacity_prompt: int, outs, staging: torch.Tensor, stream,
+                         copy_stream, events) -> None:
+    """snapkv_compress_host_layers (include/snapkv.h): layers = [(q_win, k, v)]
+    and outs = [(out_k, out_v, out_idx)] of CPU tensors (pinned for speed);
+    staging a CUDA uint8 tensor; stream / copy_stream two torch CUDA streams;
+    events four torch.cuda.Event.  Returns when every layer is complete."""
+    n = len(layers)
+    if n < 1 or len(outs) != n or len(events) != 4:
+        raise ValueError("one output triple per layer and four events")
+    q0, k0, _ = layers[0]
+    B, W, H_q, d = q0.shape
+    shape = make_shape(B, H_q, k0.shape[1], d, q0.dtype)
+    arr, _ = _seqlens_array(seqlens)
+    ptrs = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])
+    for t in [x for lay in layers for x in lay] + [x for o in outs for x in o]:
+        if not t.is_contiguous():
+            raise ValueError("every layer tensor must be contiguous")
+    for e in events:  # torch creates an event's CUDA handle when it is first recorded
+        if not e.cuda_event:
+            e.record(stream)
+    ev = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+    rc = load().snapkv_compress_host_layers(
+        ctypes.byref(shape), n, ptrs([l[0] for l in layers]), ptrs([l[1] for l in layers]),
+        ptrs([l[2] for l in layers]), arr, int(window_size), int(kernel_size),
+        pool_code(pooling), int(max_capacity_prompt), ptrs([o[0] for o in outs]),
+        ptrs([o[1] for o in outs]), ptrs([o[2] for o in outs]), staging.data_ptr(),
+        staging.numel(), _stream_handle(stream), _stream_handle(copy_stream), ev)
+    if rc:
+        raise SnapKVError(rc, "snapkv_compress_host_layers")
 
 
 def compress_noalloc(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seqlens,

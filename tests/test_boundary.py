@@ -207,3 +207,22 @@ def test_compress_ex_flags():
     r0, p0, c0 = S.score_offsets(sh, [20000], 32, 1024)
     r1, p1, c1 = S.score_offsets(sh, [20000], 32, 1024, S.PER_QUERY_HEAD)
     assert c1 == 4 * c0
+
+
+def test_host_layers_entry_point_checks_arguments():
+    """Argument errors return before any CUDA call (so this runs without a GPU)."""
+    lib = S.load()
+    shape = S.make_shape(1, 8, 2, 64, S.BF16)
+    sl = (ctypes.c_int32 * 1)(3000)
+    one = S.host_staging_size_layers(shape, [3000], 16, 256)
+    assert one >= 2 * S.host_staging_size(shape, [3000], 16, 256)
+    fake = 0x10000
+    ptrs = (ctypes.c_void_p * 1)(fake)
+    ev = (ctypes.c_void_p * 4)(fake, fake, fake, fake)
+    call = lambda n, events: lib.snapkv_compress_host_layers(
+        ctypes.byref(shape), n, ptrs, ptrs, ptrs, sl, 16, 5, 0, 256, ptrs, ptrs, ptrs, 0x10000,
+        one, None, None, events)
+    assert call(0, ev) == S.ERR_INVALID_ARG
+    assert call(1, None) == S.ERR_INVALID_ARG
+    ev0 = (ctypes.c_void_p * 4)(fake, fake, None, fake)
+    assert call(1, ev0) == S.ERR_INVALID_ARG

@@ -181,3 +181,31 @@ def test_many_kv_heads_stay_on_tensor_cores():
     assert paths == [2, 0]
     ora = parity.oracle_for(lay, 7, "max", 1024, seqs=[0, 16])
     parity.check(lay, gpu, ora, 1024, seqs=[0, 16])
+
+
+@pytest.mark.parametrize("pinned_v", [True, False])
+def test_host_layers_entry_point_matches_device(pinned_v):
+    """snapkv_compress_host_layers overlaps each layer's upload with the
+    previous layer's compression; every layer's outputs must equal the device
+    entry point's on the same inputs, bit for bit."""
+    C, W = 1024, 32
+    lays = [synth.make_inputs(20 + l, [4000, 700], 32, 8, 128, W, "bf16", nspans=4)
+            for l in range(3)]
+    ref = [parity.run_gpu(lay, 7, "avg", C) for lay in lays]
+    pin = lambda x: torch.from_numpy(x).view(torch.bfloat16).pin_memory()
+    layers = [(pin(l.q_win), pin(l.k), pin(l.v) if pinned_v
+               else torch.from_numpy(l.v.copy()).view(torch.bfloat16)) for l in lays]
+    B, H_kv, d = 2, 8, 128
+    outs = [(torch.empty((B, C, H_kv, d), dtype=torch.bfloat16).pin_memory(),
+             torch.empty((B, C, H_kv, d), dtype=torch.bfloat16).pin_memory(),
+             torch.empty((B, H_kv, C), dtype=torch.int32).pin_memory()) for _ in lays]
+    shape = S.make_shape(B, 32, H_kv, d, S.BF16)
+    staging = torch.empty(S.host_staging_size_layers(shape, lays[0].seqlens, W, C),
+                          dtype=torch.uint8, device="cuda")
+    events = [torch.cuda.Event() for _ in range(4)]
+    S.compress_host_layers(layers, lays[0].seqlens, W, 7, "avg", C, outs, staging,
+                           torch.cuda.current_stream(), torch.cuda.Stream(), events)
+    for (ok, ov, oi), r in zip(outs, ref):
+        np.testing.assert_array_equal(oi.numpy(), r["idx"])
+        np.testing.assert_array_equal(ok.view(torch.int16).numpy().view(np.uint16), r["out_k"])
+        np.testing.assert_array_equal(ov.view(torch.int16).numpy().view(np.uint16), r["out_v"])
