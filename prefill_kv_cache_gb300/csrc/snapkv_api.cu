@@ -179,7 +179,7 @@ const char* snapkv_status_string(int status) {
   }
 }
 
-int snapkv_version(void) { return 0x000200; }
+int snapkv_version(void) { return 0x000300; }
 
 size_t snapkv_workspace_size(const snapkv_shape* shape, const int32_t* seqlens_host, int32_t W,
                              int32_t C) {
