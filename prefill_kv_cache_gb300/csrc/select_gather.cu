@@ -12,11 +12,15 @@
 //      What You are Looking for Before Generation", "기술적 접근법".  The
 //      raw scores are staged in shared memory tile by tile, the pooled slice
 //      stays there for the next steps;
-//   2. find the exact n-th largest pooled value T by a three-digit radix
-//      select over the fp32 bit patterns (scores are >= 0, so the unsigned
-//      patterns order like the values).  Per-digit histograms are summed
-//      across the cluster through distributed shared memory: each CTA
-//      reduces a share of the bins, then every CTA reads the reduced bins;
+//   2. find the exact n-th largest pooled value T by a radix select over the
+//      fp32 bit patterns (scores are >= 0, so the unsigned patterns order
+//      like the values).  The first digit (11 bits) is histogrammed over the
+//      cluster through distributed shared memory: each CTA adds its counts
+//      into the owners' bins, then every CTA reads the reduced bins.  The
+//      values of the threshold bin are then gathered on rank 0, which
+//      finishes the select over them alone (two more digits) and hands every
+//      CTA the threshold and its counts; a bin too large to gather takes the
+//      two digits over the cluster instead;
 //   3. keep every position with a value above T and the lowest-positioned
 //      `need` positions equal to T (ties go to the lower position), in
 //      ascending order, via per-CTA counts and block prefix scans -- no sort;
@@ -46,6 +50,9 @@ constexpr int kMaxCluster = 16;
 constexpr int kPoolTile = 8192;                // raw scores staged per pooling step
 constexpr int kLd = 16;                        // independent global loads in flight per thread
 constexpr int kStageFloats = 44 * 1024;         // dynamic shared memory, in floats
+// values of the first digit's threshold bin that rank 0 selects from alone
+// (one word each, in its raw-staging area, which holds at least kPoolTile)
+constexpr int kCandCap = kPoolTile;
 static_assert(kMaxRows < kChunk, "window rows are copied in one pass");
 
 // Floats of the raw-score staging area for pooling half-width r: the tile,
@@ -134,6 +141,42 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
   return before + x - v;
 }
 
+// Calls f(x, pat(x)) for x = xa .. xb - 1 in order, the patterns read 8 at
+// a time ahead of their use (independent shared-memory loads in flight).
+template <typename Pat, typename F>
+__device__ __forceinline__ void walk(Pat pat, int xa, int xb, F f) {
+  for (int x0 = xa; x0 < xb; x0 += 8) {
+    unsigned u[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) u[k] = x0 + k < xb ? pat(x0 + k) : 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (x0 + k < xb) f(x0 + k, u[k]);
+  }
+}
+
+// Histogram of one radix digit: for x in [xa, xb) with (pat(x) & mask) ==
+// prefix, bin (pat(x) >> shift) & (nb - 1) of h gains one.  A thread walks
+// consecutive positions and adds each run of equal digits with one atomic
+// (neighbouring pooled scores mostly share their leading digit, so this
+// avoids most of the same-address conflicts of one atomic per value).
+template <typename Pat>
+__device__ __forceinline__ void run_hist(Pat pat, int xa, int xb, unsigned prefix, unsigned mask,
+                                         int shift, int nb, unsigned* h) {
+  int rb = -1;
+  unsigned rc = 0;
+  walk(pat, xa, xb, [&](int, unsigned u) {
+    const int bin = (u & mask) == prefix ? (int)((u >> shift) & (unsigned)(nb - 1)) : -1;
+    if (bin != rb) {
+      if (rb >= 0) atomicAdd(&h[rb], rc);
+      rb = bin;
+      rc = 0;
+    }
+    ++rc;
+  });
+  if (rb >= 0) atomicAdd(&h[rb], rc);
+}
+
 // Exclusive block scans of two values at once; returns a's prefix, writes
 // b's prefix and both totals.
 __device__ __forceinline__ int block_excl_scan2(int a, int b, int* wsum, int* a_total,
@@ -170,6 +213,38 @@ __device__ __forceinline__ int block_excl_scan2(int a, int b, int* wsum, int* a_
   *b_total = yt;
   *b_excl = yb + y - b;
   return xb + x - a;
+}
+
+// The digit D of the nb-bin histogram h with count(> D) < need <= count(>= D),
+// bins scanned from the top (4 per thread, nb <= 4 * blockDim.x).  Every
+// thread of the block calls it; *digit, *above = count(> D) and *in_bin =
+// count(D) are valid in all threads on return.
+__device__ __forceinline__ void top_digit(const unsigned* h, int nb, int need, int* wsum, int* digit,
+                                          int* above, int* in_bin) {
+  const int t = threadIdx.x;
+  int local[4], lsum = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int rb = 4 * t + q;
+    local[q] = rb < nb ? (int)h[nb - 1 - rb] : 0;
+    lsum += local[q];
+  }
+  int total;
+  const int excl = block_excl_scan(lsum, wsum, &total);
+  if (excl < need && need <= excl + lsum) {
+    int cum = excl;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (cum + local[q] >= need) {
+        *digit = nb - 1 - (4 * t + q);
+        *above = cum;
+        *in_bin = local[q];
+        break;
+      }
+      cum += local[q];
+    }
+  }
+  __syncthreads();
 }
 
 // Copy `cnt` rows: source position pos[i] of the sequence (KV head sh) ->
@@ -303,8 +378,11 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
   __shared__ unsigned hl[2048];  // this CTA's counts of the current digit, then all bins
   __shared__ int wsum[2 * kWarps];
   __shared__ int sel_pos[kChunk];
-  __shared__ int sh_digit, sh_above;
+  __shared__ int sh_digit, sh_above, sh_in_bin, sh_base;
   __shared__ int cl_cnt[2 * kMaxCluster];        // (above, equal) per CTA, on rank 0
+  __shared__ int cq[2 * kMaxCluster];            // rank 0: candidates above / equal per CTA
+  __shared__ int cand_n;                         // rank 0: candidates gathered
+  __shared__ int sel_info[4];                    // T, need, out_before, eq_before from rank 0
   __shared__ __align__(8) uint64_t bulk_bar;
 
   cg::cluster_group cluster = cg::this_cluster();
@@ -356,6 +434,8 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
   // the digit histograms start at zero in every CTA before any CTA adds to
   // them: zero, arrive on the cluster barrier now, wait after pooling
   for (int b = t; b < 3 * 2048; b += blockDim.x) (&hb[0][0])[b] = 0u;
+  if (t < 2 * kMaxCluster) cq[t] = 0;
+  if (t == 0) cand_n = 0;
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   const int Sz = (P + CS - 1) / CS;
   const int j0 = min(P, rank * Sz), j1 = min(P, j0 + Sz);
@@ -418,19 +498,22 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
 
   // the cluster barrier armed before pooling: every CTA's histograms are zero
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-  const int lane = t & 31;
-  // positions per thread for the counting and compaction passes: an odd
-  // stride, so that the threads of a warp reading their i-th positions hit
-  // 32 different shared-memory banks
+  // positions per thread for the histogram, counting and compaction passes:
+  // an odd stride, so that the threads of a warp reading their i-th
+  // positions hit 32 different shared-memory banks
   const int per = ((cnt + (int)blockDim.x - 1) / (int)blockDim.x) | 1;
   const int xa = min(cnt, t * per), xb = min(cnt, xa + per);      // this thread's range
-  int out_before = 0, eq_before = 0, need = n, my_gt = 0, my_eq = 0;
-  int excl_gt = 0, excl_eq = 0;
+  int out_before = 0, eq_before = 0, need = n;
   unsigned T = 0;
   if (n > 0) {
-    // 2. radix select of the n-th largest value (digits of 11, 11 and 10
-    //    bits of the fp32 pattern), one cluster barrier per digit
+    auto pat = [&](int x) { return __float_as_uint(vals[x]); };
+    // 2. radix select of the n-th largest value over the fp32 patterns:
+    //    digits of 11 (bits 31..21), 11 and 10 bits, each histogram summed
+    //    over the cluster with one cluster barrier.  After the first digit,
+    //    when the threshold bin holds at most kCandCap values, the rest of
+    //    the select runs on rank 0 over those candidates alone (2b).
     unsigned prefix = 0, mask = 0;
+    bool gathered = false;
     for (int pass = 0; pass < 3; ++pass) {
       const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
       const int nb = pass == 2 ? 1024 : 2048;
@@ -438,31 +521,9 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
       unsigned* hd = hb[pass];
       for (int b = t; b < nb; b += blockDim.x) hl[b] = 0u;
       __syncthreads();
-      // this CTA's counts: most lanes of a warp share one bin (scores bunch
-      // in a few exponents), so lane 0 keeps a running count of its warp's
-      // lanes in lane 0's bin and adds it only when that bin changes; the
-      // other lanes add one each
-      int run_bin = -1;
-      unsigned run_cnt = 0;
-      for (int x0 = 0; x0 < cnt; x0 += blockDim.x) {
-        const int x = x0 + t;
-        const unsigned u = x < cnt ? __float_as_uint(vals[x]) : 0u;
-        const int bin = (x < cnt && (u & mask) == prefix) ? (int)((u >> shift) & (nb - 1)) : -1;
-        const int b0 = __shfl_sync(0xffffffffu, bin, 0);
-        const unsigned same = __ballot_sync(0xffffffffu, bin == b0);
-        if (lane == 0 && b0 >= 0) {
-          if (b0 != run_bin) {
-            if (run_bin >= 0) atomicAdd(&hl[run_bin], run_cnt);
-            run_bin = b0;
-            run_cnt = 0;
-          }
-          run_cnt += (unsigned)__popc(same);
-        }
-        if (bin >= 0 && bin != b0) atomicAdd(&hl[bin], 1u);
-      }
-      if (lane == 0 && run_bin >= 0) atomicAdd(&hl[run_bin], run_cnt);
+      run_hist(pat, xa, xb, prefix, mask, shift, nb, hl);
       __syncthreads();
-      // its non-empty bins go to their owners
+      // this CTA's non-empty bins go to their owners
       for (int b = t; b < nb; b += blockDim.x) {
         const unsigned c = hl[b];
         if (c) atomicAdd(cluster.map_shared_rank(hd, b / own) + b, c);
@@ -480,62 +541,132 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
           if (b1 + u * blockDim.x < nb) hl[b1 + u * blockDim.x] = m4[u];
       }
       __syncthreads();
-      // digit D with count(> D) < need <= count(>= D); bins scanned from the top
-      int local[4], lsum = 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int rb = 4 * t + q;
-        local[q] = rb < nb ? (int)hl[nb - 1 - rb] : 0;
-        lsum += local[q];
-      }
-      int total;
-      const int excl = block_excl_scan(lsum, wsum, &total);
-      if (excl < need && need <= excl + lsum) {
-        int cum = excl;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (cum + local[q] >= need) {
-            sh_digit = nb - 1 - (4 * t + q);
-            sh_above = cum;
-            break;
-          }
-          cum += local[q];
-        }
-      }
-      __syncthreads();
+      top_digit(hl, nb, need, wsum, &sh_digit, &sh_above, &sh_in_bin);
       need -= sh_above;
       prefix |= (unsigned)sh_digit << shift;
       mask |= (unsigned)(nb - 1) << shift;
+      if (pass == 0 && sh_in_bin <= kCandCap) {  // the same decision in every CTA
+        gathered = true;
+        // hl (read by top_digit before its closing barrier) starts rank 0's
+        // candidate histogram at zero; the second digit uses hb[1], which
+        // no CTA touches on this path
+        for (int b = t; b < nb; b += blockDim.x) hl[b] = 0u;
+        break;
+      }
     }
-    T = prefix;
 
-    // 3. this CTA's values above / equal to T, per thread over its range of
-    //    consecutive positions, then across the CTA and the cluster
+    if (gathered) {
+      // 2b. the values of the threshold bin, packed as (CTA rank << 21 | low
+      //     21 bits), go to rank 0's raw-staging area (free after pooling);
+      //     the values above the bin are counted per CTA
+      const unsigned D1 = prefix >> 21;
+      unsigned* cand = reinterpret_cast<unsigned*>(sraw);
+      int nc = 0, na = 0;
+      walk(pat, xa, xb, [&](int, unsigned u) {
+        nc += (u >> 21) == D1;
+        na += (u >> 21) > D1;
+      });
+      int tot_c, tot_a, excl_a;
+      const int excl_c = block_excl_scan2(nc, na, wsum, &tot_c, &excl_a, &tot_a);
+      if (t == 0) {
+        sh_base = atomicAdd(cluster.map_shared_rank(&cand_n, 0), tot_c);
+        cluster.map_shared_rank(cl_cnt, 0)[2 * rank] = tot_a;
+      }
+      __syncthreads();
+      unsigned* dst = cluster.map_shared_rank(cand, 0) + sh_base + excl_c;
+      walk(pat, xa, xb, [&](int, unsigned u) {
+        if ((u >> 21) == D1) *dst++ = ((unsigned)rank << 21) | (u & 0x1FFFFFu);
+      });
+      cluster.sync();
+      if (rank == 0) {
+        // the last two digits (bits 20..10, 9..0) over the candidates alone
+        const int nc_all = cand_n;
+        const int cper = ((nc_all + (int)blockDim.x - 1) / (int)blockDim.x) | 1;
+        const int ca = min(nc_all, t * cper), cb = min(nc_all, ca + cper);
+        auto low = [&](int i) { return cand[i] & 0x1FFFFFu; };
+        unsigned p2 = 0, m2 = 0;
+        for (int pass = 0; pass < 2; ++pass) {
+          const int shift = pass == 0 ? 10 : 0;
+          const int nb = pass == 0 ? 2048 : 1024;
+          unsigned* hc = pass == 0 ? hl : hb[1];  // both zero here
+          run_hist(low, ca, cb, p2, m2, shift, nb, hc);
+          __syncthreads();
+          top_digit(hc, nb, need, wsum, &sh_digit, &sh_above, &sh_in_bin);
+          need -= sh_above;
+          p2 |= (unsigned)sh_digit << shift;
+          m2 |= (unsigned)(nb - 1) << shift;
+        }
+        // candidates above / equal to the threshold, per source CTA (runs of
+        // one key added at once: a CTA's candidates are contiguous)
+        int rk = -1, rc = 0;
+        walk([&](int i) { return cand[i]; }, ca, cb, [&](int, unsigned w) {
+          const unsigned v = w & 0x1FFFFFu;
+          const int key = v > p2 ? 2 * (int)(w >> 21) : (v == p2 ? 2 * (int)(w >> 21) + 1 : -1);
+          if (key != rk) {
+            if (rk >= 0) atomicAdd(&cq[rk], rc);
+            rk = key;
+            rc = 0;
+          }
+          ++rc;
+        });
+        if (rk >= 0) atomicAdd(&cq[rk], rc);
+        __syncthreads();
+        if (t < CS) {  // CTA t's kept values before its own, and equal values before its own
+          int eq_acc = 0, ob = 0, eb = 0;
+          for (int q = 0; q < CS; ++q) {
+            const int g_ = cl_cnt[2 * q] + cq[2 * q], e_ = cq[2 * q + 1];
+            const int take = min(max(need - eq_acc, 0), e_);
+            if (q < t) {
+              ob += g_ + take;
+              eb += e_;
+            }
+            eq_acc += e_;
+          }
+          int* info = cluster.map_shared_rank(sel_info, t);
+          info[0] = (int)(prefix | p2);
+          info[1] = need;
+          info[2] = ob;
+          info[3] = eb;
+        }
+      }
+      cluster.sync();
+      T = (unsigned)sel_info[0];
+      need = sel_info[1];
+      out_before = sel_info[2];
+      eq_before = sel_info[3];
+    } else {
+      T = prefix;
+    }
+
+    // 3. this thread's values above / equal to T, then across the CTA
     int gt = 0, eq = 0;
-    for (int x = xa; x < xb; ++x) {
-      const unsigned u = __float_as_uint(vals[x]);
+    walk(pat, xa, xb, [&](int, unsigned u) {
       gt += u > T;
       eq += u == T;
-    }
-    excl_gt = block_excl_scan2(gt, eq, wsum, &my_gt, &excl_eq, &my_eq);
-    if (t == 0) {
-      int* dst = cluster.map_shared_rank(cl_cnt, 0);
-      dst[2 * rank] = my_gt;
-      dst[2 * rank + 1] = my_eq;
-    }
-    cluster.sync();
-    // every CTA's pair, fetched in parallel (one remote load per thread)
-    if (t < 2 * CS) wsum[t] = cluster.map_shared_rank(cl_cnt, 0)[t];
-    __syncthreads();
-    int eq_acc = 0;
-    for (int q = 0; q < CS; ++q) {
-      const int g_ = wsum[2 * q], e_ = wsum[2 * q + 1];
-      const int take = min(max(need - eq_acc, 0), e_);
-      if (q < rank) {
-        out_before += g_ + take;
-        eq_before += e_;
+    });
+    int my_gt, my_eq, excl_eq;
+    const int excl_gt = block_excl_scan2(gt, eq, wsum, &my_gt, &excl_eq, &my_eq);
+    if (!gathered) {
+      // the CTA's counts go to rank 0, every CTA reads them all back
+      if (t == 0) {
+        int* dcl = cluster.map_shared_rank(cl_cnt, 0);
+        dcl[2 * rank] = my_gt;
+        dcl[2 * rank + 1] = my_eq;
       }
-      eq_acc += e_;
+      cluster.sync();
+      // every CTA's pair, fetched in parallel (one remote load per thread)
+      if (t < 2 * CS) wsum[t] = cluster.map_shared_rank(cl_cnt, 0)[t];
+      __syncthreads();
+      int eq_acc = 0;
+      for (int q = 0; q < CS; ++q) {
+        const int g_ = wsum[2 * q], e_ = wsum[2 * q + 1];
+        const int take = min(max(need - eq_acc, 0), e_);
+        if (q < rank) {
+          out_before += g_ + take;
+          eq_before += e_;
+        }
+        eq_acc += e_;
+      }
     }
 
     // 4. ascending compaction: a thread's kept positions go to consecutive
@@ -543,15 +674,14 @@ select_gather(const __grid_constant__ Plan p, int cap_floats) {
     //    kept in position order while the cluster still needs them
     int slot = out_before + excl_gt + min(max(need - eq_before, 0), excl_eq);
     int eq_rank = eq_before + excl_eq;
-    for (int x = xa; x < xb; ++x) {
-      const unsigned u = __float_as_uint(vals[x]);
+    walk(pat, xa, xb, [&](int x, unsigned u) {
       const bool keep = u > T || (u == T && eq_rank < need);
       eq_rank += u == T;
       if (keep) {
         if (slot < n) idx_out[slot] = j0 + x;  // slots from n on belong to the window
         ++slot;
       }
-    }
+    });
   }
 
   // 5. the window rows: slots n .. C-1 take positions P .. L-1

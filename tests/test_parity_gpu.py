@@ -49,10 +49,13 @@ def test_small_shapes(case):
     _run_and_check(lay, kp, pool, C)
 
 
+@pytest.mark.parametrize("L", [3000, 20000])
 @pytest.mark.parametrize("pool", ["avg", "max"])
-def test_exact_ties_zero_queries(pool):
-    """q = 0 makes every raw score equal: the tie rule alone decides."""
-    W, L, C, kp = 16, 3000, 512, 5
+def test_exact_ties_zero_queries(pool, L):
+    """q = 0 makes every raw score equal: the tie rule alone decides.  At
+    L = 20000 the threshold's first-digit bin holds more values than one CTA
+    gathers, so the select runs all three digits over the cluster."""
+    W, C, kp = 16, 512, 5
     lay = synth.make_inputs(5, [L, L + 7], 8, 2, 128, W, "bf16", nspans=2)
     lay.q_win[:] = 0
     gpu = parity.run_gpu(lay, kp, pool, C)
@@ -61,6 +64,19 @@ def test_exact_ties_zero_queries(pool):
     for b in range(2):
         for h in range(2):
             assert gpu["idx"][b, h, :n].tolist() == want
+
+
+@pytest.mark.parametrize("seqlens", [[12000, 9000], [30000]])
+def test_near_uniform_scores(seqlens):
+    """Tiny queries make the attention nearly uniform: all scores share one
+    first-digit bin far beyond what one CTA gathers, and the cluster-wide
+    digits decide among values a few ulps apart (checked against the oracle)."""
+    W, C, kp = 32, 2048, 7
+    lay = synth.make_inputs(31, seqlens, 16, 4, 128, W, "bf16", nspans=0)
+    lay.q_win[:] = synth.bf16_round(synth.bf16_to_f32(lay.q_win) * np.float32(1e-3))
+    gpu = parity.run_gpu(lay, kp, "avg", C)
+    ora = parity.oracle_for(lay, kp, "avg", C)
+    parity.check(lay, gpu, ora, C)
 
 
 @pytest.mark.parametrize("name", ["1", "2"])
