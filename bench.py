@@ -3,8 +3,15 @@
 
 One step = the whole compression (scores, pooling, selection, emission) of
 every layer of the workload, each layer with its own K/V, through the C ABI
-(snapkv_compress) on device-resident inputs.  The metric is prompt tokens
-compressed per second per layer, all heads: (prompt tokens x layers) / time.
+on device-resident inputs: one snapkv_compress_layers call, which runs
+consecutive layers on two streams so that a layer's selection overlaps the
+next layer's scoring.  The metric is prompt tokens compressed per second per
+layer, all heads: (prompt tokens x layers) / time.  The step is captured once
+in a CUDA graph and the timed region replays it (every replay runs every
+memset and kernel of every layer); the step issued directly
+(`us_per_layer_eager`) and every layer through snapkv_compress on one stream
+(`us_per_layer_single_calls`) are timed as well, and layer 0's outputs are
+checked byte for byte against snapkv_compress's.
 
 Default workload: a Llama-3-8B-shaped model at a 131072-token prompt, 32
 layers (32 query / 8 KV heads, d = 128, bf16, W = 64, avg pooling k = 13,
@@ -56,6 +63,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-scissorhands", action="store_true")
     ap.add_argument("--no-workloads", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="time the calls issued one by one instead of the captured step")
     ap.add_argument("--case", choices=["decode", "scissorhands"], default=None,
                     help="run a small fixed case for a profiler and exit (no timing)")
     return ap.parse_args()
@@ -279,11 +288,13 @@ def parity_vs_oracle(S, torch, lay, ora, cfg, dev):
             "rule": "scores 1e-7 + 1e-5 rel; sets equal outside the 1e-5 band; bytes by index"}
 
 
-def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=10):
+def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=12):
     """Every other workload of the pages' shapes through snapkv_compress (and
     snapkv_score alone), four layers in rotation so that inputs exceed L2:
-    microseconds per layer, prompt tokens/s and the fraction of the HBM
-    roofline of the algorithmic bytes."""
+    microseconds per layer through snapkv_compress_layers and through
+    snapkv_compress per layer (calls captured in a CUDA graph and replayed, and
+    the same calls issued directly), prompt tokens/s and the fraction of the
+    HBM roofline of the algorithmic bytes."""
     import synth
     from synth.device import make_layer_device
 
@@ -301,17 +312,30 @@ def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=
         ok = torch.empty((B, C, H_kv, d), dtype=dt, device=dev)
         ov, oi = torch.empty_like(ok), torch.empty((B, H_kv, C), dtype=torch.int32, device=dev)
 
-        def comp(i):
+        def comp(i, st=None):
             q, k, v, _ = layers[i % 4]
             S.compress(q, k, v, seqlens, W, kp, pool, C, out_k=ok, out_v=ov, out_idx=oi,
-                       workspace=ws)
+                       workspace=ws, stream=st)
 
-        def score(i):
+        wsl = torch.empty(S.workspace_size_layers(shape, seqlens, W, C), dtype=torch.uint8,
+                          device=dev)
+        lstreams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        levents = [torch.cuda.Event() for _ in range(3)]
+        louts = [(torch.empty_like(ok), torch.empty_like(ov), torch.empty_like(oi))
+                 for _ in range(4)]
+
+        def comp_layers(i, st=None):
+            # four layers per call: one timed "call" below is a quarter of it
+            if i % 4 == 0:
+                S.compress_layers([(l[0], l[1], l[2]) for l in layers], seqlens, W, kp, pool, C,
+                                  louts, wsl, lstreams, levents, stream=st)
+
+        def score(i, st=None):
             q, k, _, _ = layers[i % 4]
-            S.score(q, k, seqlens, W, C, ws)
+            S.score(q, k, seqlens, W, C, ws, stream=st)
 
         res = {"desc": cfg["desc"]}
-        for tag, fn in (("compress", comp), ("score", score)):
+        for tag, fn in (("compress", comp_layers), ("compress_single", comp), ("score", score)):
             for i in range(4):
                 fn(i)
             torch.cuda.synchronize()
@@ -321,8 +345,26 @@ def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=
                 fn(i)
             b.record()
             torch.cuda.synchronize()
-            res[f"us_per_layer_{tag}"] = 1e3 * a.elapsed_time(b) / reps
-        assert S.get_status(ws) == S.OK
+            res[f"us_per_layer_{tag}_eager"] = 1e3 * a.elapsed_time(b) / reps
+            # the same calls captured in a CUDA graph and replayed
+            cap = torch.cuda.Stream()
+            cap.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(cap):
+                with torch.cuda.graph(g, stream=cap):
+                    for i in range(reps):
+                        fn(i, cap)
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            a.record()
+            for _ in range(3):
+                g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            res[f"us_per_layer_{tag}"] = 1e3 * a.elapsed_time(b) / (3 * reps)
+            del g
+        assert S.get_status(ws) == S.OK and S.get_status(wsl) == S.OK
         score_bytes, compress_bytes = workload_bytes(cfg, seqlens, esz)
         us = res["us_per_layer_compress"]
         res["tokens_per_s"] = sum(seqlens) / (us / 1e6)
@@ -331,8 +373,13 @@ def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=
         res["bytes_per_layer"] = compress_bytes
         out[name] = res
         del layers
-    out["note"] = ("four layers in rotation, CUDA events around 10 calls; fractions of the "
-                   "measured HBM copy bandwidth for the algorithmic bytes")
+    out["note"] = ("four layers in rotation, 12 layer compressions per timing: compress = "
+                   "snapkv_compress_layers over the four layers (two layer streams), "
+                   "compress_single = snapkv_compress per layer on one stream, score = "
+                   "snapkv_score per layer; CUDA events around three replays of a CUDA graph "
+                   "of the calls (us_per_layer_*) and around the calls issued directly "
+                   "(*_eager); fractions of the measured HBM copy bandwidth for the "
+                   "algorithmic bytes, from the graph timings")
     return out
 
 
@@ -423,35 +470,105 @@ def main():
     calls = [(q.data_ptr(), k.data_ptr(), v.data_ptr(), ok.data_ptr(), ov.data_ptr(), oi.data_ptr())
              for (q, k, v), (ok, ov, oi) in zip(data, outs)]
 
-    def step():
+    def single_calls():
+        """Every layer through snapkv_compress, one after another on one stream."""
         for qp, kp_, vp, okp, ovp, oip in calls:
             rc = lib.snapkv_compress(sh_ref, qp, kp_, vp, sl_arr, W, kp, pool_code, C, okp, ovp,
                                      oip, ws_ptr, ws_len, st)
             if rc:
                 raise S.SnapKVError(rc, "snapkv_compress")
 
+    # the step: all layers in one snapkv_compress_layers call (consecutive
+    # layers on two streams, so that a layer's selection overlaps the next
+    # layer's scoring)
+    wsl = torch.empty(S.workspace_size_layers(shape, seqlens, W, C), dtype=torch.uint8, device=dev)
+    layer_streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    layer_events = [torch.cuda.Event() for _ in range(3)]
+    for e in layer_events:
+        e.record(stream)
+    arrs = [(ctypes.c_void_p * layers)(*[c[j] for c in calls]) for j in range(6)]
+    ls_arr = (ctypes.c_void_p * 2)(*[x.cuda_stream for x in layer_streams])
+    ev_arr = (ctypes.c_void_p * 3)(*[e.cuda_event for e in layer_events])
+
+    def step():
+        rc = lib.snapkv_compress_layers(sh_ref, layers, arrs[0], arrs[1], arrs[2], sl_arr, W, kp,
+                                        pool_code, C, arrs[3], arrs[4], arrs[5], wsl.data_ptr(),
+                                        wsl.numel(), st, ls_arr, ev_arr)
+        if rc:
+            raise S.SnapKVError(rc, "snapkv_compress_layers")
+
     def barrier():
         if world > 1:
             dist.barrier()
 
+    # every layer through snapkv_compress on one stream: warm-up, timing and
+    # the reference outputs of layer 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(max(3, args.warmup)):
+        single_calls()
+    torch.cuda.synchronize()
+    assert S.get_status(ws) == S.OK
+    e0.record(stream)
+    for _ in range(max(1, args.steps // 2)):
+        single_calls()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    single_ms = e0.elapsed_time(e1) / max(1, args.steps // 2)
+    ref0 = [t.clone() for t in outs[0]]
+
+    # the step issued directly
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
-    assert S.get_status(ws) == S.OK
+    assert S.get_status(wsl) == S.OK
+    e0.record(stream)
+    for _ in range(max(1, args.steps // 2)):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1) / max(1, args.steps // 2)
+    for a, b in zip(outs[0], ref0):
+        assert torch.equal(a, b), "snapkv_compress_layers differs from snapkv_compress"
+
+    # the same calls captured once (launches recorded at capture time)
+    graph = None
+    if not args.eager:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        n_cap = S.kernel_launches()
+        with torch.cuda.stream(cap):
+            st = cap.cuda_stream
+            with torch.cuda.graph(graph, stream=cap):
+                step()
+            st = stream.cuda_stream
+        per_step_launches = S.kernel_launches() - n_cap
+        for t in outs[0]:
+            t.zero_()
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert S.get_status(wsl) == S.OK
+        for a, b in zip(outs[0], ref0):
+            assert torch.equal(a, b), "a replayed layer differs from snapkv_compress's"
 
     sampler = ClockSampler(local_rank)
     barrier()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n0 = S.kernel_launches()
     sampler.start()
     e0.record(stream)
     for _ in range(args.steps):
-        step()
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
     e1.record(stream)
     torch.cuda.synchronize()
     sampler.stop()
-    launches = S.kernel_launches() - n0
+    launches = (per_step_launches * args.steps if graph is not None
+                else S.kernel_launches() - n0)
+    assert S.get_status(wsl) == S.OK
     barrier()
     ms = replica_ms(e0.elapsed_time(e1) / args.steps, world, dev)
     value = replica_value(sum(seqlens) * layers, world, ms)
@@ -518,6 +635,11 @@ def main():
                 "workload": f"{name}: {cfg['desc']}",
                 "seqlens": seqlens if len(seqlens) <= 16 else len(seqlens),
                 "layers": layers, "us_per_layer": 1e3 * ms / layers,
+                "step": "one snapkv_compress_layers call over all layers (two layer streams)",
+                "timing": "the step captured in a CUDA graph, replayed" if graph is not None
+                          else "the step issued directly",
+                "us_per_layer_eager": 1e3 * eager_ms / layers,
+                "us_per_layer_single_calls": 1e3 * single_ms / layers,
                 "l2": "inputs larger than L2 (each layer's K and V: "
                       f"{2 * sum(seqlens) * H_kv * d * esz / 1e6:.0f} MB)",
                 "parallelism": f"replicas x{world}" if world > 1 else "single GPU",

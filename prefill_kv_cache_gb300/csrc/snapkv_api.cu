@@ -222,7 +222,7 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
             int32_t C, void* out_k, void* out_v, int32_t* out_idx, void* workspace,
             size_t workspace_bytes, void* stream, bool score_only, const float* lse_in,
             bool per_q = false, const void* q_all = nullptr, const float* lse_all = nullptr,
-            bool v_zero_copy = false) {
+            bool v_zero_copy = false, int* status_word = nullptr) {
   int rc = check_problem(shape, seqlens_host, W, C);
   if (rc == SNAPKV_ERR_INVALID_ARG) return rc;
   if (!q_win || !k || !workspace) return SNAPKV_ERR_INVALID_ARG;
@@ -243,10 +243,12 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
   char* ws = static_cast<char*>(workspace);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // one memset per call: the status word and the work-queue counters, which
-  // sit together at the start of the workspace
+  // sit together at the start of the workspace (the counters alone when the
+  // caller keeps a status word of its own across several calls)
   static_assert(sizeof(int) * kCounterInts % 4 == 0, "counter region");
-  if (cudaMemsetAsync(ws + lay.status, 0, lay.counters + sizeof(int) * kCounterInts - lay.status,
-                      st) != cudaSuccess)
+  const size_t clear0 = status_word ? lay.counters : lay.status;
+  if (cudaMemsetAsync(ws + clear0, 0, lay.counters + sizeof(int) * kCounterInts - clear0, st) !=
+      cudaSuccess)
     return SNAPKV_ERR_CUDA;
   int counter_off = 0;
 
@@ -283,7 +285,7 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
   p.v_zero_copy = v_zero_copy ? 1 : 0;
   p.out_heads = per_q ? p.H_q : H;
   p.head_div = per_q ? p.g : 1;
-  p.status = reinterpret_cast<int*>(ws + lay.status);
+  p.status = status_word ? status_word : reinterpret_cast<int*>(ws + lay.status);
   p.counters = reinterpret_cast<int*>(ws + lay.counters);
   p.batch = shape->batch;
   p.total_rows = 0;
@@ -329,6 +331,62 @@ int snapkv_compress(const snapkv_shape* shape, const void* q_win, const void* k,
                     void* workspace, size_t workspace_bytes, void* stream) {
   return enqueue(shape, q_win, k, v, seqlens_host, W, kernel_size, pool_type, C, out_k, out_v,
                  out_idx, workspace, workspace_bytes, stream, false, nullptr);
+}
+
+size_t snapkv_workspace_size_layers(const snapkv_shape* shape, const int32_t* seqlens_host,
+                                    int32_t W, int32_t C) {
+  if (check_problem(shape, seqlens_host, W, C) != SNAPKV_OK) return 0;
+  return 2 * align_up(layout_for(shape, seqlens_host, W, C).total);
+}
+
+int snapkv_compress_layers(const snapkv_shape* shape, int32_t n_layers,
+                           const void* const* q_win, const void* const* k, const void* const* v,
+                           const int32_t* seqlens_host, int32_t W, int32_t kernel_size,
+                           int32_t pool_type, int32_t C, void* const* out_k, void* const* out_v,
+                           int32_t* const* out_idx, void* workspace, size_t workspace_bytes,
+                           void* stream, void* const* layer_streams, void* const* events) {
+  int rc = check_problem(shape, seqlens_host, W, C);
+  if (rc != SNAPKV_OK) return rc;
+  if (n_layers < 1 || !q_win || !k || !v || !out_k || !out_v || !out_idx || !workspace ||
+      !aligned(workspace, kAlign) || !layer_streams || !events)
+    return SNAPKV_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l)
+    if (!q_win[l] || !k[l] || !v[l] || !out_k[l] || !out_v[l] || !out_idx[l])
+      return SNAPKV_ERR_INVALID_ARG;
+  if (!layer_streams[0] || !layer_streams[1] || layer_streams[0] == layer_streams[1])
+    return SNAPKV_ERR_INVALID_ARG;
+  for (int e = 0; e < 3; ++e)
+    if (!events[e]) return SNAPKV_ERR_INVALID_ARG;
+  const size_t half = align_up(layout_for(shape, seqlens_host, W, C).total);
+  if (workspace_bytes < 2 * half) return SNAPKV_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t ls[2] = {static_cast<cudaStream_t>(layer_streams[0]),
+                        static_cast<cudaStream_t>(layer_streams[1])};
+  cudaEvent_t fork = static_cast<cudaEvent_t>(events[0]);
+  cudaEvent_t join[2] = {static_cast<cudaEvent_t>(events[1]), static_cast<cudaEvent_t>(events[2])};
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);  // the first half's status word serves the call
+  // clear it, then fork both layer streams off the caller's stream
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess ||
+      cudaEventRecord(fork, st) != cudaSuccess ||
+      cudaStreamWaitEvent(ls[0], fork, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(ls[1], fork, 0) != cudaSuccess)
+    return SNAPKV_ERR_CUDA;
+  // layer l runs on stream l % 2 in workspace half l % 2: a layer's
+  // selection overlaps the next layer's scoring on the other stream
+  int first_err = SNAPKV_OK;
+  for (int l = 0; l < n_layers && first_err == SNAPKV_OK; ++l) {
+    const int h = l & 1;
+    first_err = enqueue(shape, q_win[l], k[l], v[l], seqlens_host, W, kernel_size, pool_type, C,
+                        out_k[l], out_v[l], out_idx[l], ws + h * half, half, ls[h], false,
+                        nullptr, false, nullptr, nullptr, false, status);
+  }
+  // join, whatever happened above: the caller's stream waits for both
+  for (int h = 0; h < 2; ++h)
+    if (cudaEventRecord(join[h], ls[h]) != cudaSuccess ||
+        cudaStreamWaitEvent(st, join[h], 0) != cudaSuccess)
+      return SNAPKV_ERR_CUDA;
+  return first_err;
 }
 
 int snapkv_score(const snapkv_shape* shape, const void* q_win, const void* k,

@@ -42,6 +42,8 @@ EXPORTED = (
     "snapkv_compress_host",
     "snapkv_host_staging_size_layers",
     "snapkv_compress_host_layers",
+    "snapkv_workspace_size_layers",
+    "snapkv_compress_layers",
     "snapkv_compress_noalloc",
     "snapkv_noalloc_get_status",
     "snapkv_kernel_launches",
@@ -123,6 +125,11 @@ def load() -> ctypes.CDLL:
     lib.snapkv_compress_host_layers.argtypes = [shp, i32, vp, vp, vp, vp, i32, i32, i32, i32,
                                                 vp, vp, vp, vp, sz, vp, vp, vp]
     lib.snapkv_compress_host_layers.restype = ctypes.c_int
+    lib.snapkv_workspace_size_layers.argtypes = [shp, vp, i32, i32]
+    lib.snapkv_workspace_size_layers.restype = sz
+    lib.snapkv_compress_layers.argtypes = [shp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp,
+                                           vp, vp, sz, vp, vp, vp]
+    lib.snapkv_compress_layers.restype = ctypes.c_int
     lib.snapkv_compress_noalloc.argtypes = [shp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                             vp]
     lib.snapkv_compress_noalloc.restype = ctypes.c_int
@@ -413,6 +420,63 @@ def compress_host_layers(layers, seqlens, window_size: int, kernel_size: int, po
         staging.numel(), _stream_handle(stream), _stream_handle(copy_stream), ev)
     if rc:
         raise SnapKVError(rc, "snapkv_compress_host_layers")
+
+
+def workspace_size_layers(shape: snapkv_shape, seqlens, window_size: int,
+                          max_capacity_prompt: int) -> int:
+    arr, _ = _seqlens_array(seqlens)
+    return int(load().snapkv_workspace_size_layers(ctypes.byref(shape), arr, int(window_size),
+                                                   int(max_capacity_prompt)))
+
+
+def compress_layers(layers, seqlens, window_size: int, kernel_size: int, pooling,
+                    max_capacity_prompt: int, outs, workspace: torch.Tensor, layer_streams,
+                    events, stream=None) -> None:
+    """snapkv_compress_layers (include/snapkv.h): layers = [(q_win, k, v)] and
+    outs = [(out_k, out_v, out_idx)] of CUDA tensors, one triple per layer;
+    workspace a CUDA uint8 tensor of workspace_size_layers bytes;
+    layer_streams two torch CUDA streams, events three torch.cuda.Event.
+    Asynchronous on `stream` (default: the current stream)."""
+    n = len(layers)
+    if n < 1 or len(outs) != n or len(layer_streams) != 2 or len(events) != 3:
+        raise ValueError("one output triple per layer, two layer streams and three events")
+    q0, k0, _ = layers[0]
+    B, W, H_q, d = q0.shape
+    H_kv = k0.shape[1]
+    if W != int(window_size):
+        raise ValueError("q_win's second dimension must equal window_size")
+    C = int(max_capacity_prompt)
+    shape = make_shape(B, H_q, H_kv, d, q0.dtype)
+    for (q, k, v), (ok, ov, oi) in zip(layers, outs):
+        for name, t in (("q_win", q), ("k", k), ("v", v), ("out_k", ok), ("out_v", ov),
+                        ("out_idx", oi)):
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"every layer's {name} must be a contiguous CUDA tensor")
+        if tuple(q.shape) != (B, W, H_q, d) or tuple(k.shape) != tuple(k0.shape) or \
+                tuple(v.shape) != tuple(k0.shape):
+            raise ValueError("every layer must have the first layer's shapes")
+        if tuple(ok.shape) != (B, C, H_kv, d) or tuple(ov.shape) != (B, C, H_kv, d) or \
+                tuple(oi.shape) != (B, H_kv, C):
+            raise ValueError("output shapes must be [B, C, H_kv, d] and [B, H_kv, C]")
+        if q.dtype != q0.dtype or k.dtype != q0.dtype or v.dtype != q0.dtype or \
+                ok.dtype != q0.dtype or ov.dtype != q0.dtype or oi.dtype != torch.int32:
+            raise ValueError("inputs and out_k / out_v share one dtype; out_idx is int32")
+    st = torch.cuda.current_stream() if stream is None else stream
+    for e in events:  # torch creates an event's CUDA handle when it is first recorded
+        if not e.cuda_event:
+            e.record(st)
+    arr, _ = _seqlens_array(seqlens)
+    ptrs = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])
+    sts = (ctypes.c_void_p * 2)(*[s.cuda_stream for s in layer_streams])
+    ev = (ctypes.c_void_p * 3)(*[e.cuda_event for e in events])
+    rc = load().snapkv_compress_layers(
+        ctypes.byref(shape), n, ptrs([l[0] for l in layers]), ptrs([l[1] for l in layers]),
+        ptrs([l[2] for l in layers]), arr, int(window_size), int(kernel_size),
+        pool_code(pooling), C, ptrs([o[0] for o in outs]), ptrs([o[1] for o in outs]),
+        ptrs([o[2] for o in outs]), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream_handle(st), sts, ev)
+    if rc:
+        raise SnapKVError(rc, "snapkv_compress_layers")
 
 
 def compress_noalloc(q_win: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seqlens,

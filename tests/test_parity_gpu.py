@@ -225,3 +225,50 @@ def test_host_layers_entry_point_matches_device(pinned_v):
         np.testing.assert_array_equal(oi.numpy(), r["idx"])
         np.testing.assert_array_equal(ok.view(torch.int16).numpy().view(np.uint16), r["out_k"])
         np.testing.assert_array_equal(ov.view(torch.int16).numpy().view(np.uint16), r["out_v"])
+
+
+@pytest.mark.parametrize("n_layers,graph", [(1, False), (5, False), (4, True)])
+def test_layers_entry_point_matches_single_calls(n_layers, graph):
+    """snapkv_compress_layers runs consecutive layers on two streams with two
+    workspace halves; every layer's outputs must equal snapkv_compress on the
+    same layer, bit for bit, also when the call is captured in a CUDA graph
+    and replayed."""
+    C, W, kp = 1024, 32, 7
+    seqlens = [4000, 700, 2600]
+    lays = [synth.make_inputs(40 + l, seqlens, 32, 8, 128, W, "bf16", nspans=4)
+            for l in range(n_layers)]
+    dev = lambda x: torch.from_numpy(x).view(torch.bfloat16).cuda()
+    layers = [(dev(l.q_win), dev(l.k), dev(l.v)) for l in lays]
+    B, H_kv, d = len(seqlens), 8, 128
+    new_outs = lambda: [(torch.empty((B, C, H_kv, d), dtype=torch.bfloat16, device="cuda"),
+                         torch.empty((B, C, H_kv, d), dtype=torch.bfloat16, device="cuda"),
+                         torch.empty((B, H_kv, C), dtype=torch.int32, device="cuda"))
+                        for _ in lays]
+    ref = []
+    for q, k, v in layers:
+        ok, ov, oi, _ = S.compress(q, k, v, seqlens, W, kp, "avg", C)
+        ref.append((ok, ov, oi))
+    shape = S.make_shape(B, 32, H_kv, d, S.BF16)
+    ws = torch.empty(S.workspace_size_layers(shape, seqlens, W, C), dtype=torch.uint8,
+                     device="cuda")
+    outs = new_outs()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    events = [torch.cuda.Event() for _ in range(3)]
+    if graph:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                S.compress_layers(layers, seqlens, W, kp, "avg", C, outs, ws, streams, events,
+                                  stream=cap)
+        for _ in range(2):
+            g.replay()
+    else:
+        S.compress_layers(layers, seqlens, W, kp, "avg", C, outs, ws, streams, events)
+    torch.cuda.synchronize()
+    assert S.get_status(ws) == S.OK
+    for l, ((ok, ov, oi), (rk, rv, ri)) in enumerate(zip(outs, ref)):
+        assert torch.equal(oi, ri), l
+        assert torch.equal(ok, rk), l
+        assert torch.equal(ov, rv), l
