@@ -4,8 +4,8 @@
 One step = the whole compression (scores, pooling, selection, emission) of
 every layer of the workload, each layer with its own K/V, through the C ABI
 on device-resident inputs: one snapkv_compress_layers call, which runs
-consecutive layers on two streams so that a layer's selection overlaps the
-next layer's scoring.  The metric is prompt tokens compressed per second per
+consecutive layers on three streams (--layer-streams) so that a layer's
+selection overlaps the next layers' scoring.  The metric is prompt tokens compressed per second per
 layer, all heads: (prompt tokens x layers) / time.  The step is captured once
 in a CUDA graph and the timed region replays it (every replay runs every
 memset and kernel of every layer); the step issued directly
@@ -63,6 +63,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-scissorhands", action="store_true")
     ap.add_argument("--no-workloads", action="store_true")
+    ap.add_argument("--layer-streams", type=int, default=3,
+                    help="streams snapkv_compress_layers overlaps consecutive layers on (1-4)")
     ap.add_argument("--eager", action="store_true",
                     help="time the calls issued one by one instead of the captured step")
     ap.add_argument("--case", choices=["decode", "scissorhands"], default=None,
@@ -288,7 +290,8 @@ def parity_vs_oracle(S, torch, lay, ora, cfg, dev):
             "rule": "scores 1e-7 + 1e-5 rel; sets equal outside the 1e-5 band; bytes by index"}
 
 
-def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=12):
+def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=12,
+                   layer_streams=3):
     """Every other workload of the pages' shapes through snapkv_compress (and
     snapkv_score alone), four layers in rotation so that inputs exceed L2:
     microseconds per layer through snapkv_compress_layers and through
@@ -317,10 +320,10 @@ def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=
             S.compress(q, k, v, seqlens, W, kp, pool, C, out_k=ok, out_v=ov, out_idx=oi,
                        workspace=ws, stream=st)
 
-        wsl = torch.empty(S.workspace_size_layers(shape, seqlens, W, C), dtype=torch.uint8,
-                          device=dev)
-        lstreams = [torch.cuda.Stream(), torch.cuda.Stream()]
-        levents = [torch.cuda.Event() for _ in range(3)]
+        wsl = torch.empty(S.workspace_size_layers(shape, seqlens, W, C, layer_streams),
+                          dtype=torch.uint8, device=dev)
+        lstreams = [torch.cuda.Stream() for _ in range(layer_streams)]
+        levents = [torch.cuda.Event() for _ in range(layer_streams + 1)]
         louts = [(torch.empty_like(ok), torch.empty_like(ov), torch.empty_like(oi))
                  for _ in range(4)]
 
@@ -374,7 +377,7 @@ def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=
         out[name] = res
         del layers
     out["note"] = ("four layers in rotation, 12 layer compressions per timing: compress = "
-                   "snapkv_compress_layers over the four layers (two layer streams), "
+                   f"snapkv_compress_layers over the four layers ({layer_streams} layer streams), "
                    "compress_single = snapkv_compress per layer on one stream, score = "
                    "snapkv_score per layer; CUDA events around three replays of a CUDA graph "
                    "of the calls (us_per_layer_*) and around the calls issued directly "
@@ -481,19 +484,21 @@ def main():
     # the step: all layers in one snapkv_compress_layers call (consecutive
     # layers on two streams, so that a layer's selection overlaps the next
     # layer's scoring)
-    wsl = torch.empty(S.workspace_size_layers(shape, seqlens, W, C), dtype=torch.uint8, device=dev)
-    layer_streams = [torch.cuda.Stream(), torch.cuda.Stream()]
-    layer_events = [torch.cuda.Event() for _ in range(3)]
+    ns = args.layer_streams
+    wsl = torch.empty(S.workspace_size_layers(shape, seqlens, W, C, ns), dtype=torch.uint8,
+                      device=dev)
+    layer_streams = [torch.cuda.Stream() for _ in range(ns)]
+    layer_events = [torch.cuda.Event() for _ in range(ns + 1)]
     for e in layer_events:
         e.record(stream)
     arrs = [(ctypes.c_void_p * layers)(*[c[j] for c in calls]) for j in range(6)]
-    ls_arr = (ctypes.c_void_p * 2)(*[x.cuda_stream for x in layer_streams])
-    ev_arr = (ctypes.c_void_p * 3)(*[e.cuda_event for e in layer_events])
+    ls_arr = (ctypes.c_void_p * ns)(*[x.cuda_stream for x in layer_streams])
+    ev_arr = (ctypes.c_void_p * (ns + 1))(*[e.cuda_event for e in layer_events])
 
     def step():
         rc = lib.snapkv_compress_layers(sh_ref, layers, arrs[0], arrs[1], arrs[2], sl_arr, W, kp,
                                         pool_code, C, arrs[3], arrs[4], arrs[5], wsl.data_ptr(),
-                                        wsl.numel(), st, ls_arr, ev_arr)
+                                        wsl.numel(), st, ns, ls_arr, ev_arr)
         if rc:
             raise S.SnapKVError(rc, "snapkv_compress_layers")
 
@@ -617,7 +622,7 @@ def main():
 
     workloads = None
     if rank == 0 and name == "4" and not args.no_workloads:
-        workloads = workload_table(S, torch, dev, peak)
+        workloads = workload_table(S, torch, dev, peak, layer_streams=ns)
 
     cpu, parity = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -635,7 +640,7 @@ def main():
                 "workload": f"{name}: {cfg['desc']}",
                 "seqlens": seqlens if len(seqlens) <= 16 else len(seqlens),
                 "layers": layers, "us_per_layer": 1e3 * ms / layers,
-                "step": "one snapkv_compress_layers call over all layers (two layer streams)",
+                "step": f"one snapkv_compress_layers call over all layers ({ns} layer streams)",
                 "timing": "the step captured in a CUDA graph, replayed" if graph is not None
                           else "the step issued directly",
                 "us_per_layer_eager": 1e3 * eager_ms / layers,

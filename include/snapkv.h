@@ -246,14 +246,14 @@ int snapkv_score_offsets(const snapkv_shape *shape, const int32_t *seqlens_host,
 
 /*
  * Several device-resident layers in one call, consecutive layers overlapping:
- * layer l is enqueued on layer_streams[l % 2] with its own half of the
- * workspace, so that one layer's selection (a short, latency-bound kernel
- * that leaves most SMs idle) runs while the next layer is scored on the other
- * stream.  Same outputs, bit for bit, as snapkv_compress on each layer.  The
- * call forks both layer streams off `stream` (events[0]) and joins them back
- * (events[1], events[2]), so work enqueued on `stream` afterwards sees every
- * layer's outputs; it works under stream capture.  Asynchronous; nothing is
- * allocated.
+ * layer l is enqueued on layer_streams[l % n_streams] with its own part of
+ * the workspace, so that one layer's selection (a short, latency-bound kernel
+ * that leaves most SMs idle) and the tail of its scoring run while the next
+ * layers are scored on the other streams.  Same outputs, bit for bit, as
+ * snapkv_compress on each layer.  The call forks the layer streams off
+ * `stream` (events[0]) and joins them back (events[1 .. n_streams]), so work
+ * enqueued on `stream` afterwards sees every layer's outputs; it works under
+ * stream capture.  Asynchronous; nothing is allocated.
  *
  *   n_layers       >= 1
  *   q_win, k, v    host arrays of n_layers device pointers, each a layer's
@@ -261,27 +261,34 @@ int snapkv_score_offsets(const snapkv_shape *shape, const int32_t *seqlens_host,
  *                  seqlens_host, W, kernel_size, pool_type and C)
  *   out_k, out_v, out_idx  host arrays of n_layers device pointers
  *   workspace      device, 256-byte aligned, >= snapkv_workspace_size_layers
- *                  bytes (two single-layer workspaces back to back)
+ *                  bytes for n_streams (n_streams single-layer workspaces
+ *                  back to back)
  *   stream         the caller's cudaStream_t
- *   layer_streams  array of 2 distinct cudaStream_t of the current device,
- *                  owned by the caller (non-blocking streams recommended)
- *   events         array of 3 cudaEvent_t created by the caller (the library
- *                  creates none)
+ *   n_streams      1 .. SNAPKV_MAX_LAYER_STREAMS (2 or 3 overlap best)
+ *   layer_streams  array of n_streams distinct cudaStream_t of the current
+ *                  device, owned by the caller (non-blocking streams
+ *                  recommended)
+ *   events         array of n_streams + 1 cudaEvent_t created by the caller
+ *                  (the library creates none)
  * One status word serves the whole call: snapkv_get_status on `workspace`
  * reports SNAPKV_ERR_TIMEOUT if any layer's bounded device wait gave up.
  * Returns SNAPKV_OK once every layer is enqueued, or the error of the first
  * layer that could not be (the streams are joined either way); argument
- * errors return before anything is enqueued.
+ * errors return before anything is enqueued.  snapkv_workspace_size_layers
+ * returns 0 for an invalid problem or n_streams.
  */
+#define SNAPKV_MAX_LAYER_STREAMS 4
+
 size_t snapkv_workspace_size_layers(const snapkv_shape *shape, const int32_t *seqlens_host,
-                                    int32_t W, int32_t C);
+                                    int32_t W, int32_t C, int32_t n_streams);
 
 int snapkv_compress_layers(const snapkv_shape *shape, int32_t n_layers,
                            const void *const *q_win, const void *const *k, const void *const *v,
                            const int32_t *seqlens_host, int32_t W, int32_t kernel_size,
                            int32_t pool_type, int32_t C, void *const *out_k, void *const *out_v,
                            int32_t *const *out_idx, void *workspace, size_t workspace_bytes,
-                           void *stream, void *const *layer_streams, void *const *events);
+                           void *stream, int32_t n_streams, void *const *layer_streams,
+                           void *const *events);
 
 /*
  * Synchronize `stream`, then read the device status word that the kernels

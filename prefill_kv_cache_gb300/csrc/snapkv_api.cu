@@ -334,9 +334,10 @@ int snapkv_compress(const snapkv_shape* shape, const void* q_win, const void* k,
 }
 
 size_t snapkv_workspace_size_layers(const snapkv_shape* shape, const int32_t* seqlens_host,
-                                    int32_t W, int32_t C) {
+                                    int32_t W, int32_t C, int32_t n_streams) {
   if (check_problem(shape, seqlens_host, W, C) != SNAPKV_OK) return 0;
-  return 2 * align_up(layout_for(shape, seqlens_host, W, C).total);
+  if (n_streams < 1 || n_streams > SNAPKV_MAX_LAYER_STREAMS) return 0;
+  return (size_t)n_streams * align_up(layout_for(shape, seqlens_host, W, C).total);
 }
 
 int snapkv_compress_layers(const snapkv_shape* shape, int32_t n_layers,
@@ -344,48 +345,53 @@ int snapkv_compress_layers(const snapkv_shape* shape, int32_t n_layers,
                            const int32_t* seqlens_host, int32_t W, int32_t kernel_size,
                            int32_t pool_type, int32_t C, void* const* out_k, void* const* out_v,
                            int32_t* const* out_idx, void* workspace, size_t workspace_bytes,
-                           void* stream, void* const* layer_streams, void* const* events) {
+                           void* stream, int32_t n_streams, void* const* layer_streams,
+                           void* const* events) {
   int rc = check_problem(shape, seqlens_host, W, C);
   if (rc != SNAPKV_OK) return rc;
   if (n_layers < 1 || !q_win || !k || !v || !out_k || !out_v || !out_idx || !workspace ||
-      !aligned(workspace, kAlign) || !layer_streams || !events)
+      !aligned(workspace, kAlign) || n_streams < 1 || n_streams > SNAPKV_MAX_LAYER_STREAMS ||
+      !layer_streams || !events)
     return SNAPKV_ERR_INVALID_ARG;
   for (int l = 0; l < n_layers; ++l)
     if (!q_win[l] || !k[l] || !v[l] || !out_k[l] || !out_v[l] || !out_idx[l])
       return SNAPKV_ERR_INVALID_ARG;
-  if (!layer_streams[0] || !layer_streams[1] || layer_streams[0] == layer_streams[1])
-    return SNAPKV_ERR_INVALID_ARG;
-  for (int e = 0; e < 3; ++e)
+  for (int i = 0; i < n_streams; ++i) {
+    if (!layer_streams[i]) return SNAPKV_ERR_INVALID_ARG;
+    for (int j = 0; j < i; ++j)
+      if (layer_streams[i] == layer_streams[j]) return SNAPKV_ERR_INVALID_ARG;
+  }
+  for (int e = 0; e <= n_streams; ++e)
     if (!events[e]) return SNAPKV_ERR_INVALID_ARG;
-  const size_t half = align_up(layout_for(shape, seqlens_host, W, C).total);
-  if (workspace_bytes < 2 * half) return SNAPKV_ERR_WORKSPACE;
+  const size_t part = align_up(layout_for(shape, seqlens_host, W, C).total);
+  if (workspace_bytes < (size_t)n_streams * part) return SNAPKV_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaStream_t ls[2] = {static_cast<cudaStream_t>(layer_streams[0]),
-                        static_cast<cudaStream_t>(layer_streams[1])};
   cudaEvent_t fork = static_cast<cudaEvent_t>(events[0]);
-  cudaEvent_t join[2] = {static_cast<cudaEvent_t>(events[1]), static_cast<cudaEvent_t>(events[2])};
   char* ws = static_cast<char*>(workspace);
-  int* status = reinterpret_cast<int*>(ws);  // the first half's status word serves the call
-  // clear it, then fork both layer streams off the caller's stream
+  int* status = reinterpret_cast<int*>(ws);  // the first part's status word serves the call
+  // clear it, then fork the layer streams off the caller's stream
   if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess ||
-      cudaEventRecord(fork, st) != cudaSuccess ||
-      cudaStreamWaitEvent(ls[0], fork, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(ls[1], fork, 0) != cudaSuccess)
+      cudaEventRecord(fork, st) != cudaSuccess)
     return SNAPKV_ERR_CUDA;
-  // layer l runs on stream l % 2 in workspace half l % 2: a layer's
-  // selection overlaps the next layer's scoring on the other stream
+  for (int i = 0; i < n_streams; ++i)
+    if (cudaStreamWaitEvent(static_cast<cudaStream_t>(layer_streams[i]), fork, 0) != cudaSuccess)
+      return SNAPKV_ERR_CUDA;
+  // layer l runs on stream l % n_streams in workspace part l % n_streams: a
+  // layer's selection overlaps the next layers' scoring on the other streams
   int first_err = SNAPKV_OK;
   for (int l = 0; l < n_layers && first_err == SNAPKV_OK; ++l) {
-    const int h = l & 1;
+    const int h = l % n_streams;
     first_err = enqueue(shape, q_win[l], k[l], v[l], seqlens_host, W, kernel_size, pool_type, C,
-                        out_k[l], out_v[l], out_idx[l], ws + h * half, half, ls[h], false,
-                        nullptr, false, nullptr, nullptr, false, status);
+                        out_k[l], out_v[l], out_idx[l], ws + h * part, part, layer_streams[h],
+                        false, nullptr, false, nullptr, nullptr, false, status);
   }
-  // join, whatever happened above: the caller's stream waits for both
-  for (int h = 0; h < 2; ++h)
-    if (cudaEventRecord(join[h], ls[h]) != cudaSuccess ||
-        cudaStreamWaitEvent(st, join[h], 0) != cudaSuccess)
+  // join, whatever happened above: the caller's stream waits for every one
+  for (int i = 0; i < n_streams; ++i) {
+    cudaEvent_t join = static_cast<cudaEvent_t>(events[1 + i]);
+    if (cudaEventRecord(join, static_cast<cudaStream_t>(layer_streams[i])) != cudaSuccess ||
+        cudaStreamWaitEvent(st, join, 0) != cudaSuccess)
       return SNAPKV_ERR_CUDA;
+  }
   return first_err;
 }
 

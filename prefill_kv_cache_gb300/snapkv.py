@@ -125,10 +125,10 @@ def load() -> ctypes.CDLL:
     lib.snapkv_compress_host_layers.argtypes = [shp, i32, vp, vp, vp, vp, i32, i32, i32, i32,
                                                 vp, vp, vp, vp, sz, vp, vp, vp]
     lib.snapkv_compress_host_layers.restype = ctypes.c_int
-    lib.snapkv_workspace_size_layers.argtypes = [shp, vp, i32, i32]
+    lib.snapkv_workspace_size_layers.argtypes = [shp, vp, i32, i32, i32]
     lib.snapkv_workspace_size_layers.restype = sz
     lib.snapkv_compress_layers.argtypes = [shp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp,
-                                           vp, vp, sz, vp, vp, vp]
+                                           vp, vp, sz, vp, i32, vp, vp]
     lib.snapkv_compress_layers.restype = ctypes.c_int
     lib.snapkv_compress_noalloc.argtypes = [shp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                             vp]
@@ -422,11 +422,14 @@ def compress_host_layers(layers, seqlens, window_size: int, kernel_size: int, po
         raise SnapKVError(rc, "snapkv_compress_host_layers")
 
 
+MAX_LAYER_STREAMS = 4
+
+
 def workspace_size_layers(shape: snapkv_shape, seqlens, window_size: int,
-                          max_capacity_prompt: int) -> int:
+                          max_capacity_prompt: int, n_streams: int = 2) -> int:
     arr, _ = _seqlens_array(seqlens)
     return int(load().snapkv_workspace_size_layers(ctypes.byref(shape), arr, int(window_size),
-                                                   int(max_capacity_prompt)))
+                                                   int(max_capacity_prompt), int(n_streams)))
 
 
 def compress_layers(layers, seqlens, window_size: int, kernel_size: int, pooling,
@@ -434,12 +437,15 @@ def compress_layers(layers, seqlens, window_size: int, kernel_size: int, pooling
                     events, stream=None) -> None:
     """snapkv_compress_layers (include/snapkv.h): layers = [(q_win, k, v)] and
     outs = [(out_k, out_v, out_idx)] of CUDA tensors, one triple per layer;
-    workspace a CUDA uint8 tensor of workspace_size_layers bytes;
-    layer_streams two torch CUDA streams, events three torch.cuda.Event.
-    Asynchronous on `stream` (default: the current stream)."""
+    layer_streams 1 .. MAX_LAYER_STREAMS torch CUDA streams; workspace a CUDA
+    uint8 tensor of workspace_size_layers(..., len(layer_streams)) bytes;
+    events len(layer_streams) + 1 torch.cuda.Event.  Asynchronous on
+    `stream` (default: the current stream)."""
     n = len(layers)
-    if n < 1 or len(outs) != n or len(layer_streams) != 2 or len(events) != 3:
-        raise ValueError("one output triple per layer, two layer streams and three events")
+    ns = len(layer_streams)
+    if n < 1 or len(outs) != n or not 1 <= ns <= MAX_LAYER_STREAMS or len(events) != ns + 1:
+        raise ValueError("one output triple per layer, 1 .. 4 layer streams and one event "
+                         "more than streams")
     q0, k0, _ = layers[0]
     B, W, H_q, d = q0.shape
     H_kv = k0.shape[1]
@@ -467,14 +473,14 @@ def compress_layers(layers, seqlens, window_size: int, kernel_size: int, pooling
             e.record(st)
     arr, _ = _seqlens_array(seqlens)
     ptrs = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])
-    sts = (ctypes.c_void_p * 2)(*[s.cuda_stream for s in layer_streams])
-    ev = (ctypes.c_void_p * 3)(*[e.cuda_event for e in events])
+    sts = (ctypes.c_void_p * ns)(*[s.cuda_stream for s in layer_streams])
+    ev = (ctypes.c_void_p * (ns + 1))(*[e.cuda_event for e in events])
     rc = load().snapkv_compress_layers(
         ctypes.byref(shape), n, ptrs([l[0] for l in layers]), ptrs([l[1] for l in layers]),
         ptrs([l[2] for l in layers]), arr, int(window_size), int(kernel_size),
         pool_code(pooling), C, ptrs([o[0] for o in outs]), ptrs([o[1] for o in outs]),
         ptrs([o[2] for o in outs]), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), _stream_handle(st), sts, ev)
+        workspace.numel() * workspace.element_size(), _stream_handle(st), ns, sts, ev)
     if rc:
         raise SnapKVError(rc, "snapkv_compress_layers")
 

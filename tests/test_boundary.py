@@ -235,27 +235,41 @@ def test_layers_entry_point_checks_arguments():
     shape = S.make_shape(1, 8, 2, 64, S.BF16)
     sl = (ctypes.c_int32 * 1)(3000)
     single = S.workspace_size(shape, [3000], 16, 256)
-    both = S.workspace_size_layers(shape, [3000], 16, 256)
-    assert both >= 2 * single and both % 256 == 0
+    for ns in (1, 2, 3, 4):
+        size = S.workspace_size_layers(shape, [3000], 16, 256, ns)
+        assert size >= ns * single and size % 256 == 0
+    assert S.workspace_size_layers(shape, [3000], 16, 256, 0) == 0
+    assert S.workspace_size_layers(shape, [3000], 16, 256, 5) == 0
+    both = S.workspace_size_layers(shape, [3000], 16, 256, 2)
     fake = 0x10000
     ptrs = (ctypes.c_void_p * 2)(fake, fake)
     sts = (ctypes.c_void_p * 2)(0x100, 0x200)
     ev = (ctypes.c_void_p * 3)(fake, fake, fake)
 
-    def call(n, streams=sts, events=ev, ws_bytes=both, p=ptrs):
+    def call(n, streams=sts, events=ev, ws_bytes=both, p=ptrs, ns=2):
         return lib.snapkv_compress_layers(ctypes.byref(shape), n, p, p, p, sl, 16, 5, 0, 256, p,
-                                          p, p, 0x10000, ws_bytes, None, streams, events)
+                                          p, p, 0x10000, ws_bytes, None, ns, streams, events)
 
     assert call(0) == S.ERR_INVALID_ARG
+    assert call(1, ns=0) == S.ERR_INVALID_ARG
+    assert call(1, ns=5) == S.ERR_INVALID_ARG
     assert call(1, streams=None) == S.ERR_INVALID_ARG
     assert call(1, events=None) == S.ERR_INVALID_ARG
     assert call(1, streams=(ctypes.c_void_p * 2)(0x100, 0x100)) == S.ERR_INVALID_ARG
+    assert call(1, streams=(ctypes.c_void_p * 2)(0x100, None)) == S.ERR_INVALID_ARG
     assert call(1, events=(ctypes.c_void_p * 3)(fake, None, fake)) == S.ERR_INVALID_ARG
     assert call(2, p=(ctypes.c_void_p * 2)(fake, None)) == S.ERR_INVALID_ARG
     assert call(2, ws_bytes=both - 256) == S.ERR_WORKSPACE
+    # three streams want three workspace parts and four events
+    three = S.workspace_size_layers(shape, [3000], 16, 256, 3)
+    sts3 = (ctypes.c_void_p * 3)(0x100, 0x200, 0x300)
+    ev4 = (ctypes.c_void_p * 4)(fake, fake, fake, None)
+    assert call(1, streams=sts3, events=ev4, ws_bytes=three, ns=3) == S.ERR_INVALID_ARG
+    ev4 = (ctypes.c_void_p * 4)(fake, fake, fake, fake)
+    assert call(1, streams=sts3, events=ev4, ws_bytes=three - 256, ns=3) == S.ERR_WORKSPACE
     # unsupported head size, before anything else
     bad = S.make_shape(1, 8, 2, 96, S.BF16)
     assert lib.snapkv_compress_layers(ctypes.byref(bad), 1, ptrs, ptrs, ptrs, sl, 16, 5, 0, 256,
-                                      ptrs, ptrs, ptrs, 0x10000, both, None, sts,
+                                      ptrs, ptrs, ptrs, 0x10000, both, None, 2, sts,
                                       ev) == S.ERR_UNSUPPORTED
-    assert S.workspace_size_layers(bad, [3000], 16, 256) == 0
+    assert S.workspace_size_layers(bad, [3000], 16, 256, 2) == 0

@@ -227,12 +227,14 @@ def test_host_layers_entry_point_matches_device(pinned_v):
         np.testing.assert_array_equal(ov.view(torch.int16).numpy().view(np.uint16), r["out_v"])
 
 
-@pytest.mark.parametrize("n_layers,graph", [(1, False), (5, False), (4, True)])
-def test_layers_entry_point_matches_single_calls(n_layers, graph):
-    """snapkv_compress_layers runs consecutive layers on two streams with two
-    workspace halves; every layer's outputs must equal snapkv_compress on the
-    same layer, bit for bit, also when the call is captured in a CUDA graph
-    and replayed."""
+@pytest.mark.parametrize("n_layers,n_streams,graph",
+                         [(1, 2, False), (5, 2, False), (4, 2, True), (7, 3, False),
+                          (6, 4, True), (3, 1, False)])
+def test_layers_entry_point_matches_single_calls(n_layers, n_streams, graph):
+    """snapkv_compress_layers runs consecutive layers on n_streams streams,
+    each with its own workspace part; every layer's outputs must equal
+    snapkv_compress on the same layer, bit for bit, also when the call is
+    captured in a CUDA graph and replayed."""
     C, W, kp = 1024, 32, 7
     seqlens = [4000, 700, 2600]
     lays = [synth.make_inputs(40 + l, seqlens, 32, 8, 128, W, "bf16", nspans=4)
@@ -249,11 +251,11 @@ def test_layers_entry_point_matches_single_calls(n_layers, graph):
         ok, ov, oi, _ = S.compress(q, k, v, seqlens, W, kp, "avg", C)
         ref.append((ok, ov, oi))
     shape = S.make_shape(B, 32, H_kv, d, S.BF16)
-    ws = torch.empty(S.workspace_size_layers(shape, seqlens, W, C), dtype=torch.uint8,
-                     device="cuda")
+    ws = torch.empty(S.workspace_size_layers(shape, seqlens, W, C, n_streams),
+                     dtype=torch.uint8, device="cuda")
     outs = new_outs()
-    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
-    events = [torch.cuda.Event() for _ in range(3)]
+    streams = [torch.cuda.Stream() for _ in range(n_streams)]
+    events = [torch.cuda.Event() for _ in range(n_streams + 1)]
     if graph:
         cap = torch.cuda.Stream()
         cap.wait_stream(torch.cuda.current_stream())
