@@ -325,13 +325,14 @@ def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=
         lstreams = [torch.cuda.Stream() for _ in range(layer_streams)]
         levents = [torch.cuda.Event() for _ in range(layer_streams + 1)]
         louts = [(torch.empty_like(ok), torch.empty_like(ov), torch.empty_like(oi))
-                 for _ in range(4)]
+                 for _ in range(reps)]
 
         def comp_layers(i, st=None):
-            # four layers per call: one timed "call" below is a quarter of it
-            if i % 4 == 0:
-                S.compress_layers([(l[0], l[1], l[2]) for l in layers], seqlens, W, kp, pool, C,
-                                  louts, wsl, lstreams, levents, stream=st)
+            # all reps layer compressions in one call (inputs rotating over
+            # the four layers): the timed "calls" below are its layers
+            if i % reps == 0:
+                S.compress_layers([layers[j % 4][:3] for j in range(reps)], seqlens, W, kp, pool,
+                                  C, louts, wsl, lstreams, levents, stream=st)
 
         def score(i, st=None):
             q, k, _, _ = layers[i % 4]
@@ -377,7 +378,7 @@ def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=
         out[name] = res
         del layers
     out["note"] = ("four layers in rotation, 12 layer compressions per timing: compress = "
-                   f"snapkv_compress_layers over the four layers ({layer_streams} layer streams), "
+                   f"one snapkv_compress_layers call over them ({layer_streams} layer streams), "
                    "compress_single = snapkv_compress per layer on one stream, score = "
                    "snapkv_score per layer; CUDA events around three replays of a CUDA graph "
                    "of the calls (us_per_layer_*) and around the calls issued directly "

@@ -141,18 +141,14 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wsum, int* total) {
   return before + x - v;
 }
 
-// Calls f(x, pat(x)) for x = xa .. xb - 1 in order, the patterns read 8 at
-// a time ahead of their use (independent shared-memory loads in flight).
+// Calls f(x, pat(x)) for x = xa .. xb - 1 in order.  Not unrolled: every
+// pass of this kernel runs once per CTA, so its code is fetched cold, and
+// short loop bodies cost less in instruction fetch than the loads they could
+// batch (measured: unrolling by 8 made the selection ~2 us slower).
 template <typename Pat, typename F>
 __device__ __forceinline__ void walk(Pat pat, int xa, int xb, F f) {
-  for (int x0 = xa; x0 < xb; x0 += 8) {
-    unsigned u[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) u[k] = x0 + k < xb ? pat(x0 + k) : 0u;
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-      if (x0 + k < xb) f(x0 + k, u[k]);
-  }
+#pragma unroll 1
+  for (int x = xa; x < xb; ++x) f(x, pat(x));
 }
 
 // Histogram of one radix digit: for x in [xa, xb) with (pat(x) & mask) ==
