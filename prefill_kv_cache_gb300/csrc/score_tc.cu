@@ -1034,7 +1034,16 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) 
     }
     // queue order: P1(0) | P1(1) M(0) | P1(2) M(1) P2(0) | ... | M(G-1) P2(G-2) | P2(G-1):
     // merges follow the next group's pass 1, pass 2 trails by two groups, so
-    // pass-2 items rarely wait for their merge while K is still in L2
+    // pass-2 items rarely wait for their merge while K is still in L2.  A
+    // launch whose pass-1 items fill at most two waves of CTAs takes every
+    // pass 1, then every merge, then every pass 2 instead: with the lagged
+    // order its first wave would park CTAs on pass-2 items of early groups
+    // (waiting for their merges) while later groups' pass-1 items wait for
+    // a CTA.  Every item waits only on items earlier in the queue either way.
+    long long p1_total = 0;
+    for (int k = 0; k < g; ++k) p1_total += tp.grp[k].p1_items;
+    const bool one_wave = p1_total <= 2LL * sms;
+    const int lag_m = one_wave ? g : 1, lag_p2 = one_wave ? 2 * g : 2;  // lag_m < lag_p2
     int idx = 0;
     if (p.lse_in) {  // the caller's LSE: pass 2 only
       for (int k = 0; k < g; ++k) {
@@ -1045,18 +1054,18 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) 
         idx += G.p2_items;
       }
     }
-    for (int k = 0; k <= g + 1 && !p.lse_in; ++k) {
+    for (int k = 0; k < g + lag_p2 && !p.lse_in; ++k) {
       if (k < g) {
         tp.grp[k].p1_start = idx;
         idx += tp.grp[k].p1_items;
       }
-      if (k >= 1 && k - 1 < g) {
-        tp.grp[k - 1].m_start = idx;
-        idx += tp.grp[k - 1].m_items;
+      if (k >= lag_m && k - lag_m < g) {
+        tp.grp[k - lag_m].m_start = idx;
+        idx += tp.grp[k - lag_m].m_items;
       }
-      if (k >= 2) {
-        tp.grp[k - 2].p2_start = idx;
-        idx += tp.grp[k - 2].p2_items;
+      if (k >= lag_p2 && k - lag_p2 < g) {
+        tp.grp[k - lag_p2].p2_start = idx;
+        idx += tp.grp[k - lag_p2].p2_items;
       }
     }
     tp.total_items = idx;
