@@ -500,30 +500,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 }
 
 // Grid (nseq, H_q), D threads: merges the chunks of one sequence and head.
-// Every chunk's (max, sum) is read once, all chunks at a time across the
-// threads; their scale factors go to shared memory; each thread then sums
-// its column over the chunks with independent loads.
-constexpr int kCombineTile = 1024;  // chunks whose scale factors sit in shared memory at once
-
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float w = __shfl_xor_sync(0xffffffffu, v, o);
-    v = is_max ? fmaxf(v, w) : v + w;
-  }
-  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  __syncthreads();  // red is free
-  if ((threadIdx.x & 31) == 0) red[warp] = v;
-  __syncthreads();
-  v = red[0];
-  for (int w = 1; w < nw; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
-  return v;
-}
+// Every thread reads every chunk's (max, sum) and its own column of every
+// chunk's output, kCombineTile chunks at a time with all loads in flight,
+// and merges them online (a running max, sum and output rescaled when the
+// max grows), so the block needs no reduction and no barrier: the whole
+// merge is about one round trip to memory per tile.
+constexpr int kCombineTile = 32;
 
 template <bool SH>
 __global__ void decode_combine(const __grid_constant__ Params p) {
-  __shared__ float fk[kCombineTile];
-  __shared__ float red[32];
   pdl_trigger();
   pdl_wait();  // every chunk's partials are written
   const int s = blockIdx.x, hq = blockIdx.y, c = threadIdx.x;
@@ -533,25 +518,32 @@ __global__ void decode_combine(const __grid_constant__ Params p) {
   const size_t ustride = (size_t)p.H_kv * p.g;                       // between chunks
   const float2* ml = p.part_ml + ((size_t)S.chunk0 * p.H_kv + h) * p.g + x;  // chunk k: ml[k * ustride]
   const float* po = p.part_o + (((size_t)S.chunk0 * p.H_kv + h) * p.g + x) * p.d + c;
-  float M = -INFINITY;
-  for (int k = c; k < nch; k += blockDim.x) M = fmaxf(M, ml[(size_t)k * ustride].x);
-  M = block_reduce(M, true, red);
-  float Lp = 0.f, O = 0.f;
+  float M = -INFINITY, L = 0.f, O = 0.f;
   for (int k0 = 0; k0 < nch; k0 += kCombineTile) {
-    const int nk = min(kCombineTile, nch - k0);
-    __syncthreads();  // the previous tile's factors are read
-    for (int k = c; k < nk; k += blockDim.x) {
-      const float2 v = ml[(size_t)(k0 + k) * ustride];
-      const float f = v.x == -INFINITY ? 0.f : ex2(v.x - M);
-      fk[k] = f;
-      Lp += v.y * f;
+    float2 v[kCombineTile];
+    float o[kCombineTile];
+#pragma unroll
+    for (int k = 0; k < kCombineTile; ++k) {
+      const bool in = k0 + k < nch;
+      v[k] = in ? __ldcg(ml + (size_t)(k0 + k) * ustride) : make_float2(-INFINITY, 0.f);
+      o[k] = in ? __ldcg(po + (size_t)(k0 + k) * ustride * p.d) : 0.f;
     }
-    __syncthreads();
-    const float* pk = po + (size_t)k0 * ustride * p.d;
-#pragma unroll 8
-    for (int k = 0; k < nk; ++k) O = fmaf(pk[(size_t)k * ustride * p.d], fk[k], O);
+    float tm = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kCombineTile; ++k) tm = fmaxf(tm, v[k].x);
+    const float Mn = fmaxf(M, tm);
+    if (Mn == -INFINITY) continue;  // no chunk with rows yet
+    const float f0 = ex2(M - Mn);   // 0 while M = -inf (L and O are 0 then)
+    L *= f0;
+    O *= f0;
+#pragma unroll
+    for (int k = 0; k < kCombineTile; ++k) {
+      const float f = v[k].x == -INFINITY ? 0.f : ex2(v[k].x - Mn);
+      L = fmaf(v[k].y, f, L);
+      O = fmaf(o[k], f, O);
+    }
+    M = Mn;
   }
-  const float L = block_reduce(Lp, false, red);
   p.out[((size_t)(p.b0 + s) * p.H_q + hq) * p.d + c] = O / L;
   if constexpr (SH) {
     if (c == 0) p.sh_ml[(size_t)(p.b0 + s) * p.H_q + hq] = make_float2(M, L);
