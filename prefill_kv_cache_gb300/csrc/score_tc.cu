@@ -49,8 +49,10 @@
 namespace snapkv {
 namespace tc {
 
-constexpr int kThreads = 384;  // 3 warpgroups
-constexpr int kConsumerThreads = 256;
+// NSG consumer super-groups of two warpgroups each (8 warps) beside the role
+// warpgroup: 1 for W * g = 128, 2 (ping-ponging over the two TMEM buffers)
+// for W * g = 256, where the longer tiles hide the hand-offs
+__host__ __device__ constexpr int threads_for(int nsg) { return 128 + 256 * nsg; }
 constexpr int kTileKeys = 128;
 constexpr int kTilesPerPiece = 8;  // at most 1024 keys per piece (the call chooses)
 constexpr int kMaxStages = 8;
@@ -59,7 +61,6 @@ constexpr int kPub = 4;  // pass-1 publication slots between consumers and the h
 constexpr int kMaxGroups = 128;
 constexpr int kGroupTiles = 1024;
 constexpr int kMinGroups = 8;  // groups per launch the sizing aims for
-constexpr int kMergeRows = 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSmemLimit = 232448;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -75,6 +76,7 @@ struct Group {
 struct TcPlan {
   int ngroups, total_items, stages, wp;
   int tpp;        // key tiles per piece (the call's piece size / 128)
+  int merge_rows; // window rows per merge item: 4 per consumer warp
   int* counters;  // [0] queue head; [1+g] pass-1 pieces done; [1+G+g] merges done
   Group grp[kMaxGroups];
 };
@@ -340,8 +342,8 @@ __device__ Entry decode(const Plan& p, const TcPlan& tp, int idx) {
     e.type = kind;
     e.g = g;
     if (kind == kMerge) {
-      e.row0 = local * kMergeRows;
-      e.nrows = min(kMergeRows, (G.u1 - G.u0) * tp.wp - e.row0);
+      e.row0 = local * tp.merge_rows;
+      e.nrows = min(tp.merge_rows, (G.u1 - G.u0) * tp.wp - e.row0);
       return e;
     }
     for (int u = G.u0; u < G.u1; ++u) {
@@ -368,11 +370,17 @@ __device__ Entry decode(const Plan& p, const TcPlan& tp, int idx) {
 // ---------------------------------------------------------- the kernel ---
 
 // PER_Q: every query head keeps its own pass-2 sums (per-query-head selection)
-template <bool PER_Q>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool PER_Q, int NSG>
+__global__ void __launch_bounds__(threads_for(NSG), 1)
 score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan tp,
                 const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  constexpr int kConsumerThreads = 256 * NSG;
+  constexpr int kConsumerWarps = kConsumerThreads / 32;
+  // registers at launch: 384 x 168 = 64512 (NSG 1) or 640 x 96 = 61440 (NSG 2);
+  // the role warpgroup drops to 40, the consumers rise to kConsumerRegs:
+  // 128 x 40 + 256 x 232 = 64512, 128 x 40 + 512 x 104 = 58368
+  constexpr int kConsumerRegs = NSG == 2 ? 104 : 232;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NS = tp.stages, wp = tp.wp, d = p.d;
   const int halves = d / 64;
@@ -394,9 +402,11 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
   uint64_t* sfull = tempty + 2;
   uint64_t* sempty = sfull + kRing;
   uint64_t* drain = sempty + kRing;  // MMA drain at teardown
-  uint64_t* pub_full = drain + 1;     // pass-1 item finished by the 8 consumer warps
+  uint64_t* pub_full = drain + 1;     // pass-1 item finished by the consumer warps
   uint64_t* pub_empty = pub_full + kPub;  // helper done with the slot
-  int* pub_grp = reinterpret_cast<int*>(pub_empty + kPub);
+  uint64_t* gl_full = pub_empty + kPub;   // per warpgroup: its pass-2 LSE copy written
+  uint64_t* gl_empty = gl_full + 4;       // per warpgroup: the copy read to the end
+  int* pub_grp = reinterpret_cast<int*>(gl_empty + 4);
   Entry* ring = reinterpret_cast<Entry*>(pub_grp + kPub);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ring + kRing);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(abort_flag) + 1);
@@ -412,16 +422,20 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       mbar_init(&qfull[b], 1);
       mbar_init(&qempty[b], 1);
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 8);  // the 8 consumer warps
+      mbar_init(&tempty[b], 8);  // the 8 warps of the super-group that reads buffer b
     }
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&sfull[s], 1);
-      mbar_init(&sempty[s], 9);  // MMA thread + 8 consumer warps
+      mbar_init(&sempty[s], 1 + kConsumerWarps);  // MMA thread + the consumer warps
     }
     mbar_init(drain, 1);
     for (int k = 0; k < kPub; ++k) {
-      mbar_init(&pub_full[k], 8);  // the consumer warps
+      mbar_init(&pub_full[k], kConsumerWarps);
       mbar_init(&pub_empty[k], 1);
+    }
+    for (int k = 0; k < 4; ++k) {
+      mbar_init(&gl_full[k], 4);   // the warpgroup's four warps
+      mbar_init(&gl_empty[k], 4);
     }
     *abort_flag = (smem_addr(smem) & 1023u) != 0 ? 1 : 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -439,10 +453,7 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const float c2 = p.log2e_scale;  // log2(e) / sqrt(d)
-  // registers: the launch gives 168 per thread (384 x 168 = 64512); the
-  // producer / MMA warpgroup hands most of its share to the consumers, who
-  // hold a tile's 128 accumulator columns in registers:
-  // 128 x 40 + 256 x 232 = 64512.  Each role's branch sets its own count.
+  // each role's branch sets its own register count (see kConsumerRegs)
 
   if (warp < 4) reg_dealloc();  // one instruction for the whole warpgroup
   if (warp == 0) {
@@ -595,29 +606,36 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
     }
   } else if (warp >= 4) {
     // ----------------------------------------------------- consumers ---
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 232;" ::: "memory");
-    const int ct = threadIdx.x - 128;         // 0..255
-    const int wg = ct >> 7;                   // warpgroup: column half it reads
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs) : "memory");
+    // two super-groups of two warpgroups: super-group sg reads the tiles of
+    // TMEM buffer sg (every other tile), its warpgroup wg the column half wg
+    const int ct = threadIdx.x - 128;         // 0..511
+    const int sg = NSG == 2 ? ct >> 8 : 0;    // super-group
+    const int wg = (ct >> 7) & 1;             // warpgroup within it: column half it reads
+    const int grp = ct >> 7;                  // warpgroup index 0..3
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int lrow = quarter * 32 + lane;     // TMEM lane of this thread
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const int R = wp / 128;
     const int half = wp >> 1;
-    int ring_n = 0, tile_n = 0;
+    int ring_n = 0, tile_n = 0, p2_n = 0;  // p2_n: pass-2 items taken (phase of gl_*)
     const uint64_t c2c2 = pk(c2, c2);
     // two 32-column chunks of a tile's accumulator (pass 1: 32 keys of one
     // query row; pass 2: 32 query rows of one key)
     uint32_t v[64];
+    // pass 2: -lse2 of the warpgroup's query rows, item-constant, one shared
+    // copy per warpgroup (written by its four warps; gl_full / gl_empty, with
+    // bounded waits, order the writes and the reads)
+    float* gl = aux + grp * 128;
     // pass 1: this thread's query row of a tile (row block wg when there are
     // two, else row block 0 with the group's half of the keys) and the row's
     // window index; both are the same for every item
     const int prow = (R == 2 ? 128 * wg : 0) + lrow;
     const int pwin = prow / p.g;
     const int kofs = R == 2 ? 0 : 64 * wg;  // first key of the group's share of a tile
-    const int cw = warp - 4;                // consumer warp 0..7
-    float* wlse = aux + cw * 64;            // this warp's copy of -lse2 for rows 64..127 of its share
+    const int cw = warp - 4;                // consumer warp 0..15
     // hands a finished pass-1 item (group g; -1: no more) to the helper warp,
-    // which publishes it with one device-scope release once all 8 consumer
+    // which publishes it with one device-scope release once all consumer
     // warps have written their statistics
     int pub_n = 0;
     auto publish = [&](int g) -> bool {
@@ -640,11 +658,12 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
         break;
       }
       const Group& G = tp.grp[e.g];
-      // partial statistics per piece and row: one per row block with two
-      // row blocks (a row has one owner), one per group with one
-      const int nslot = R == 2 ? 1 : 2;
+      // partial statistics per piece and row: one per super-group with two
+      // row blocks (a row block has one warpgroup per super-group), two per
+      // super-group with one (the warpgroups split the keys)
+      const int nslot = R == 2 ? NSG : 2 * NSG;
       if (e.type == kMerge) {
-        // each warp merges 4 of the item's 32 rows, 8 lanes per row with the
+        // each warp merges 4 of the item's 4 x kConsumerWarps rows, 8 lanes per row with the
         // partial statistics strided over them; every lane issues its loads
         // before it combines any of them
         if (lane == 0) wait_counter(&tp.counters[1 + e.g], G.p1_items, ctl);
@@ -707,48 +726,32 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
       const int s_idx = e.u / p.H_kv, h = e.u % p.H_kv;
       const SeqInfo& S = p.seq[s_idx];
       bool ok = true;
-      float nl01[64];  // pass 2: -lse2 of this thread's first 64 query rows, item-constant
       if (e.type == kP2) {
-        // the window rows' LSE (merged above, or the caller's): this warp's
-        // lanes need the rows half wg ... half wg + half - 1, the same for
-        // every lane; the first 64 go to registers, the rest to this warp's
-        // own shared-memory copy
+        // the window rows' LSE (merged above, or the caller's): the
+        // warpgroup's rows half wg ... half wg + half - 1, the same for every
+        // lane, go to its shared copy; warp quarter q writes rows 32q ...
+        // 32q + 31 once the previous item's readers are done (gl_empty)
         if (!p.lse_in && lane == 0)
-          wait_counter(&tp.counters[1 + tp.ngroups + e.g], G.m_items * 8, ctl);
+          wait_counter(&tp.counters[1 + tp.ngroups + e.g], G.m_items * kConsumerWarps, ctl);
         __syncwarp();
         if (*abort_flag) break;
+        if (!wait_bar(&gl_empty[grp], (p2_n & 1) ^ 1, ctl)) break;
         const int r0 = wg * half;  // first query row of the group's share
-        if (p.lse_in) {
-          // the caller's natural-log LSE, row r = i g + member; g divides
-          // W * g, a power of two, so it is one too
-          const int lg = __ffs(p.g) - 1;
-          const float* base = p.lse_in + (size_t)S.b * p.W * p.H_q + (size_t)h * p.g;
-#pragma unroll
-          for (int j = 0; j < 64; ++j) {
-            const int rr = r0 + j;
-            nl01[j] = -__ldg(base + (size_t)(rr >> lg) * p.H_q + (rr & (p.g - 1))) * kLog2e;
-          }
-          if (half == 128) {
-            const int ra = r0 + 64 + lane, rb = r0 + 96 + lane;
-            wlse[lane] = -__ldg(base + (size_t)(ra >> lg) * p.H_q + (ra & (p.g - 1))) * kLog2e;
-            wlse[32 + lane] = -__ldg(base + (size_t)(rb >> lg) * p.H_q + (rb & (p.g - 1))) * kLog2e;
-          }
-        } else {
-          const float4* src = reinterpret_cast<const float4*>(p.lse + (size_t)e.u * wp + r0);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float4 x = __ldcg(src + j);
-            nl01[4 * j] = -x.x;
-            nl01[4 * j + 1] = -x.y;
-            nl01[4 * j + 2] = -x.z;
-            nl01[4 * j + 3] = -x.w;
-          }
-          if (half == 128) {
-            wlse[lane] = -__ldcg(p.lse + (size_t)e.u * wp + r0 + 64 + lane);
-            wlse[32 + lane] = -__ldcg(p.lse + (size_t)e.u * wp + r0 + 96 + lane);
+        if (quarter * 32 < half) {
+          const int rr = r0 + quarter * 32 + lane;
+          if (p.lse_in) {
+            // the caller's natural-log LSE, row r = i g + member; g divides
+            // W * g, a power of two, so it is one too
+            const int lg = __ffs(p.g) - 1;
+            const float* base = p.lse_in + (size_t)S.b * p.W * p.H_q + (size_t)h * p.g;
+            gl[quarter * 32 + lane] = -__ldg(base + (size_t)(rr >> lg) * p.H_q + (rr & (p.g - 1))) * kLog2e;
+          } else {
+            gl[quarter * 32 + lane] = -__ldcg(p.lse + (size_t)e.u * wp + rr);
           }
         }
         __syncwarp();
+        if (lane == 0) mbar_arrive(&gl_full[grp]);
+        if (!wait_bar(&gl_full[grp], p2_n & 1, ctl)) break;
       }
       float Mr = -INFINITY, Zr = 0.f;  // pass 1: running reference and sum of this thread's row
       float* raw_out = p.raw + S.score0 + (size_t)h * S.P;
@@ -774,7 +777,8 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
         p1_chunk_exact(vc, lim, c2, Mr, Zr);
       };
       for (int t = 0; t < e.ntiles; ++t, ++tile_n) {
-        const int ab = tile_n & 1;  // TMEM buffer of this tile; both groups read it
+        const int ab = tile_n & 1;  // TMEM buffer of this tile; its super-group reads it
+        if (NSG == 2 && ab != sg) continue;
         if (!wait_bar(&tfull[ab], (tile_n >> 1) & 1, ctl)) {
           ok = false;
           break;
@@ -814,26 +818,26 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
           }
         } else {
           uint64_t acc[4] = {0, 0, 0, 0};
-          p2_chunk(v, nl01, c2c2, acc);
+          p2_chunk(v, gl, c2c2, acc);
           tmem_wait32(v + 32);
           if (half == 128) {
             __syncwarp();
             tmem_ld32_async(tb + 64u, v);
-            p2_chunk(v + 32, nl01 + 32, c2c2, acc);
+            p2_chunk(v + 32, gl + 32, c2c2, acc);
             tmem_wait32(v);
             __syncwarp();
             tmem_ld32_async(tb + 96u, v + 32);
-            p2_chunk(v, wlse, c2c2, acc);
+            p2_chunk(v, gl + 64, c2c2, acc);
             tmem_wait32(v + 32);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ab]);
-            p2_chunk(v + 32, wlse + 32, c2c2, acc);
+            p2_chunk(v + 32, gl + 96, c2c2, acc);
           } else {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[ab]);
-            p2_chunk(v + 32, nl01 + 32, c2c2, acc);
+            p2_chunk(v + 32, gl + 32, c2c2, acc);
           }
           const int key = key0 + lrow;
           if (PER_Q) {
@@ -879,9 +883,14 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
         // device-scope release that publishes them takes a while (it waits
         // for this warp's writes to land): the helper warp does it
         const size_t piece = (size_t)S.piece0 + (size_t)h * S.chunks + e.piece;
-        const int q = R == 2 ? 0 : wg;
+        const int q = R == 2 ? sg : 2 * sg + wg;
         p.stats[piece * 512 + (size_t)q * wp + prow] = make_float2(Mr, Zr);
         if (!publish(e.g)) break;
+      }
+      if (e.type == kP2) {  // the warpgroup's LSE copy may be overwritten
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&gl_empty[grp]);
+        ++p2_n;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[slot]);
@@ -951,7 +960,7 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) 
   const uint32_t halves = p.d / 64;
   const uint32_t q_bytes = (uint32_t)p.Wp * 128u * halves;
   const uint32_t k_bytes = (uint32_t)kTileKeys * 128u * halves;
-  const uint32_t misc = 512 * 4 + (2 * kMaxStages + 8 + 2 * kRing + 1 + 2 * kPub) * 8 +
+  const uint32_t misc = 512 * 4 + (2 * kMaxStages + 16 + 2 * kRing + 1 + 2 * kPub) * 8 +
                         kPub * 4 + kRing * sizeof(Entry) + 8;
   const long long room = (long long)kSmemLimit - 2 * (long long)q_bytes - misc;
   int stages = (int)(room / k_bytes);
@@ -966,7 +975,13 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) 
     return cudaErrorInvalidValue;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  auto kern = p.out_heads != p.H_kv ? score_tc_kernel<true> : score_tc_kernel<false>;
+  // two consumer super-groups at W * g = 256, one at 128 (the shorter tiles
+  // do not hide the ping-pong's per-item hand-offs)
+  const int nsg = p.Wp == 256 ? 2 : 1;
+  const int threads = threads_for(nsg);
+  auto kern = p.out_heads != p.H_kv
+                  ? (nsg == 2 ? score_tc_kernel<true, 2> : score_tc_kernel<true, 1>)
+                  : (nsg == 2 ? score_tc_kernel<false, 2> : score_tc_kernel<false, 1>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
@@ -1001,6 +1016,7 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) 
     std::memset(&tp, 0, sizeof tp);
     tp.wp = p.Wp;
     tp.tpp = tpp;
+    tp.merge_rows = 32 * nsg;  // 4 rows per consumer warp
     tp.counters = p.counters;
     tp.stages = stages;
     // groups of whole KV heads, ~kGroupTiles key tiles each, at most
@@ -1030,7 +1046,7 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) 
         G.p1_items += (t1 + tpp - 1) / tpp;
         G.p2_items += (t2 + tpp - 1) / tpp;
       }
-      G.m_items = ((G.u1 - G.u0) * p.Wp + kMergeRows - 1) / kMergeRows;
+      G.m_items = ((G.u1 - G.u0) * p.Wp + tp.merge_rows - 1) / tp.merge_rows;
     }
     // queue order: P1(0) | P1(1) M(0) | P1(2) M(1) P2(0) | ... | M(G-1) P2(G-2) | P2(G-1):
     // merges follow the next group's pass 1, pass 2 trails by two groups, so
@@ -1080,7 +1096,7 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) 
     tp.counters = p.counters + *counter_off;
     *counter_off += need;
     const int grid = sms < tp.total_items ? sms : tp.total_items;
-    kern<<<grid, kThreads, smem, st>>>(p, tp, tm_k, tm_q);
+    kern<<<grid, threads, smem, st>>>(p, tp, tm_k, tm_q);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launches(1);
