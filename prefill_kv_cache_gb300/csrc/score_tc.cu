@@ -104,10 +104,13 @@ __device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t bytes) {
                "r"(bytes)
                : "memory");
 }
+// One bounded try: the thread is suspended until the phase completes or a
+// 20 us hint runs out, so a waiting warp does not take issue slots from the
+// warps that work.
 __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
   uint32_t done;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 20000;\n"
       " selp.b32 %0, 1, 0, p;\n}\n"
       : "=r"(done)
       : "r"(smem_addr(b)), "r"(parity)
@@ -123,7 +126,7 @@ __device__ __forceinline__ bool wait_bar_slow(uint64_t* b, uint32_t parity, Ctl 
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test(b, parity)) return true;
-    if ((it & 63) == 0) {
+    if ((it & 15) == 0) {  // each try suspends for up to 20 us unless the phase completes
       if (*c.abort) return false;
       if (global_ns() - t0 > kWaitNs) {
         raise_timeout(c);
