@@ -4,7 +4,7 @@
 One step = the whole compression (scores, pooling, selection, emission) of
 every layer of the workload, each layer with its own K/V, through the C ABI
 on device-resident inputs: one snapkv_compress_layers call, which runs
-consecutive layers on three streams (--layer-streams) so that a layer's
+consecutive layers on four streams (--layer-streams) so that a layer's
 selection overlaps the next layers' scoring.  The metric is prompt tokens compressed per second per
 layer, all heads: (prompt tokens x layers) / time.  The step is captured once
 in a CUDA graph and the timed region replays it (every replay runs every
@@ -63,7 +63,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-scissorhands", action="store_true")
     ap.add_argument("--no-workloads", action="store_true")
-    ap.add_argument("--layer-streams", type=int, default=3,
+    ap.add_argument("--layer-streams", type=int, default=4,
                     help="streams snapkv_compress_layers overlaps consecutive layers on (1-4)")
     ap.add_argument("--eager", action="store_true",
                     help="time the calls issued one by one instead of the captured step")
@@ -291,7 +291,7 @@ def parity_vs_oracle(S, torch, lay, ora, cfg, dev):
 
 
 def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=12,
-                   layer_streams=3):
+                   layer_streams=4):
     """Every other workload of the pages' shapes through snapkv_compress (and
     snapkv_score alone), four layers in rotation so that inputs exceed L2:
     microseconds per layer through snapkv_compress_layers and through

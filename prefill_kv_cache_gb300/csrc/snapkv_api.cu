@@ -179,7 +179,7 @@ const char* snapkv_status_string(int status) {
   }
 }
 
-int snapkv_version(void) { return 0x000400; }
+int snapkv_version(void) { return 0x000401; }
 
 size_t snapkv_workspace_size(const snapkv_shape* shape, const int32_t* seqlens_host, int32_t W,
                              int32_t C) {
