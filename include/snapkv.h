@@ -247,9 +247,9 @@ int snapkv_score_offsets(const snapkv_shape *shape, const int32_t *seqlens_host,
 /*
  * Several device-resident layers in one call, consecutive layers overlapping:
  * layer l is enqueued on layer_streams[l % n_streams] with its own part of
- * the workspace, so that one layer's selection (a short, latency-bound kernel
- * that leaves most SMs idle) and the tail of its scoring run while the next
- * layers are scored on the other streams.  Same outputs, bit for bit, as
+ * the workspace, and each layer's score kernel runs on 1/n_streams of the
+ * SMs, so that n_streams layers' latency-bound scoring chains (pass 1 ->
+ * merge -> pass 2) and their selections run side by side.  Same outputs, bit for bit, as
  * snapkv_compress on each layer.  The call forks the layer streams off
  * `stream` (events[0]) and joins them back (events[1 .. n_streams]), so work
  * enqueued on `stream` afterwards sees every layer's outputs; it works under
@@ -264,7 +264,8 @@ int snapkv_score_offsets(const snapkv_shape *shape, const int32_t *seqlens_host,
  *                  bytes for n_streams (n_streams single-layer workspaces
  *                  back to back)
  *   stream         the caller's cudaStream_t
- *   n_streams      1 .. SNAPKV_MAX_LAYER_STREAMS (2 or 3 overlap best)
+ *   n_streams      1 .. SNAPKV_MAX_LAYER_STREAMS; each layer's score kernel takes
+ *                  1/n_streams of the SMs (4 measured best on GB300)
  *   layer_streams  array of n_streams distinct cudaStream_t of the current
  *                  device, owned by the caller (non-blocking streams
  *                  recommended)
@@ -277,7 +278,7 @@ int snapkv_score_offsets(const snapkv_shape *shape, const int32_t *seqlens_host,
  * errors return before anything is enqueued.  snapkv_workspace_size_layers
  * returns 0 for an invalid problem or n_streams.
  */
-#define SNAPKV_MAX_LAYER_STREAMS 4
+#define SNAPKV_MAX_LAYER_STREAMS 8
 
 size_t snapkv_workspace_size_layers(const snapkv_shape *shape, const int32_t *seqlens_host,
                                     int32_t W, int32_t C, int32_t n_streams);

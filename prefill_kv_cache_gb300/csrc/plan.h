@@ -60,6 +60,7 @@ struct Plan {
   // o gathers KV head o / head_div)
   int out_heads, head_div;
   int v_zero_copy;  // v is page-locked host memory read in place (plain loads only)
+  int gpu_share;  // n > 1: n such calls run side by side, the score kernel takes 1/n of the SMs
   int* status;       // device status word
   int* counters;     // work-queue head and per-group completion counters
   long long total_rows;  // rows of k / v in the whole call (T)

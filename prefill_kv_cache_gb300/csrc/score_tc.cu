@@ -1054,7 +1054,7 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) 
     // queue order: P1(0) | P1(1) M(0) | P1(2) M(1) P2(0) | ... | M(G-1) P2(G-2) | P2(G-1):
     // merges follow the next group's pass 1, pass 2 trails by two groups, so
     // pass-2 items rarely wait for their merge while K is still in L2.  A
-    // launch whose pass-1 items fill at most two waves of CTAs takes every
+    // launch with at most two pass-1 items per SM of the GPU takes every
     // pass 1, then every merge, then every pass 2 instead: with the lagged
     // order its first wave would park CTAs on pass-2 items of early groups
     // (waiting for their merges) while later groups' pass-1 items wait for
@@ -1098,7 +1098,10 @@ int launch_score_tc(const Plan& p, void* stream, bool* taken, int* counter_off) 
     }
     tp.counters = p.counters + *counter_off;
     *counter_off += need;
-    const int grid = sms < tp.total_items ? sms : tp.total_items;
+    // one CTA per SM, or per SM of this call's share when several calls run
+    // side by side (their waits are only on their own items: no deadlock)
+    const int width = p.gpu_share > 1 ? std::max(1, sms / p.gpu_share) : sms;
+    const int grid = width < tp.total_items ? width : tp.total_items;
     kern<<<grid, threads, smem, st>>>(p, tp, tm_k, tm_q);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -222,7 +222,7 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
             int32_t C, void* out_k, void* out_v, int32_t* out_idx, void* workspace,
             size_t workspace_bytes, void* stream, bool score_only, const float* lse_in,
             bool per_q = false, const void* q_all = nullptr, const float* lse_all = nullptr,
-            bool v_zero_copy = false, int* status_word = nullptr) {
+            bool v_zero_copy = false, int* status_word = nullptr, int gpu_share = 1) {
   int rc = check_problem(shape, seqlens_host, W, C);
   if (rc == SNAPKV_ERR_INVALID_ARG) return rc;
   if (!q_win || !k || !workspace) return SNAPKV_ERR_INVALID_ARG;
@@ -283,6 +283,7 @@ int enqueue(const snapkv_shape* shape, const void* q_win, const void* k, const v
   p.q_all = q_all;
   p.lse_all = lse_all;
   p.v_zero_copy = v_zero_copy ? 1 : 0;
+  p.gpu_share = gpu_share;
   p.out_heads = per_q ? p.H_q : H;
   p.head_div = per_q ? p.g : 1;
   p.status = status_word ? status_word : reinterpret_cast<int*>(ws + lay.status);
@@ -377,13 +378,15 @@ int snapkv_compress_layers(const snapkv_shape* shape, int32_t n_layers,
     if (cudaStreamWaitEvent(static_cast<cudaStream_t>(layer_streams[i]), fork, 0) != cudaSuccess)
       return SNAPKV_ERR_CUDA;
   // layer l runs on stream l % n_streams in workspace part l % n_streams: a
-  // layer's selection overlaps the next layers' scoring on the other streams
+  // layer's selection overlaps the next layers' scoring on the other streams,
+  // and each layer's score kernel takes 1/n_streams of the SMs, so that the
+  // layers' latency-bound pass-1 -> merge -> pass-2 chains run side by side
   int first_err = SNAPKV_OK;
   for (int l = 0; l < n_layers && first_err == SNAPKV_OK; ++l) {
     const int h = l % n_streams;
     first_err = enqueue(shape, q_win[l], k[l], v[l], seqlens_host, W, kernel_size, pool_type, C,
                         out_k[l], out_v[l], out_idx[l], ws + h * part, part, layer_streams[h],
-                        false, nullptr, false, nullptr, nullptr, false, status);
+                        false, nullptr, false, nullptr, nullptr, false, status, n_streams);
   }
   // join, whatever happened above: the caller's stream waits for every one
   for (int i = 0; i < n_streams; ++i) {

@@ -422,7 +422,7 @@ def compress_host_layers(layers, seqlens, window_size: int, kernel_size: int, po
         raise SnapKVError(rc, "snapkv_compress_host_layers")
 
 
-MAX_LAYER_STREAMS = 4
+MAX_LAYER_STREAMS = 8
 
 
 def workspace_size_layers(shape: snapkv_shape, seqlens, window_size: int,
@@ -444,7 +444,7 @@ def compress_layers(layers, seqlens, window_size: int, kernel_size: int, pooling
     n = len(layers)
     ns = len(layer_streams)
     if n < 1 or len(outs) != n or not 1 <= ns <= MAX_LAYER_STREAMS or len(events) != ns + 1:
-        raise ValueError("one output triple per layer, 1 .. 4 layer streams and one event "
+        raise ValueError("one output triple per layer, 1 .. 8 layer streams and one event "
                          "more than streams")
     q0, k0, _ = layers[0]
     B, W, H_q, d = q0.shape

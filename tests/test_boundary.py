@@ -235,11 +235,11 @@ def test_layers_entry_point_checks_arguments():
     shape = S.make_shape(1, 8, 2, 64, S.BF16)
     sl = (ctypes.c_int32 * 1)(3000)
     single = S.workspace_size(shape, [3000], 16, 256)
-    for ns in (1, 2, 3, 4):
+    for ns in range(1, S.MAX_LAYER_STREAMS + 1):
         size = S.workspace_size_layers(shape, [3000], 16, 256, ns)
         assert size >= ns * single and size % 256 == 0
     assert S.workspace_size_layers(shape, [3000], 16, 256, 0) == 0
-    assert S.workspace_size_layers(shape, [3000], 16, 256, 5) == 0
+    assert S.workspace_size_layers(shape, [3000], 16, 256, S.MAX_LAYER_STREAMS + 1) == 0
     both = S.workspace_size_layers(shape, [3000], 16, 256, 2)
     fake = 0x10000
     ptrs = (ctypes.c_void_p * 2)(fake, fake)
@@ -252,7 +252,7 @@ def test_layers_entry_point_checks_arguments():
 
     assert call(0) == S.ERR_INVALID_ARG
     assert call(1, ns=0) == S.ERR_INVALID_ARG
-    assert call(1, ns=5) == S.ERR_INVALID_ARG
+    assert call(1, ns=S.MAX_LAYER_STREAMS + 1) == S.ERR_INVALID_ARG
     assert call(1, streams=None) == S.ERR_INVALID_ARG
     assert call(1, events=None) == S.ERR_INVALID_ARG
     assert call(1, streams=(ctypes.c_void_p * 2)(0x100, 0x100)) == S.ERR_INVALID_ARG
