@@ -381,12 +381,13 @@ int snapkv_compress_layers(const snapkv_shape* shape, int32_t n_layers,
   // layer's selection overlaps the next layers' scoring on the other streams,
   // and each layer's score kernel takes 1/n_streams of the SMs, so that the
   // layers' latency-bound pass-1 -> merge -> pass-2 chains run side by side
+  const int share = std::min<int>(n_streams, n_layers);  // launches that can run side by side
   int first_err = SNAPKV_OK;
   for (int l = 0; l < n_layers && first_err == SNAPKV_OK; ++l) {
     const int h = l % n_streams;
     first_err = enqueue(shape, q_win[l], k[l], v[l], seqlens_host, W, kernel_size, pool_type, C,
                         out_k[l], out_v[l], out_idx[l], ws + h * part, part, layer_streams[h],
-                        false, nullptr, false, nullptr, nullptr, false, status, n_streams);
+                        false, nullptr, false, nullptr, nullptr, false, status, share);
   }
   // join, whatever happened above: the caller's stream waits for every one
   for (int i = 0; i < n_streams; ++i) {
