@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pdl.cuh"
@@ -53,6 +54,8 @@ constexpr int kStageFloats = 44 * 1024;         // dynamic shared memory, in flo
 // values of the first digit's threshold bin that rank 0 selects from alone
 // (one word each, in its raw-staging area, which holds at least kPoolTile)
 constexpr int kCandCap = kPoolTile;
+// pooled values per CTA below which a smaller cluster costs little latency
+constexpr int kShortSlice = 4096;
 static_assert(kMaxRows < kChunk, "window rows are copied in one pass");
 
 // Floats of the raw-score staging area for pooling half-width r: the tile,
@@ -776,6 +779,15 @@ int launch_select_gather(const Plan& p, void* stream) {
   const int room = kStageFloats - raw_span(p.kp / 2);
   int CS = 1;
   while (CS < max_cluster && (units * CS < sms || (maxP + CS - 1) / CS > room)) CS *= 2;
+  if (p.gpu_share > 1) {
+    // several calls share the GPU: clusters only large enough to fill this
+    // call's share, as long as every CTA's slice stays short (the selection's
+    // passes cost in proportion to it)
+    const int fill = std::max(1, sms / p.gpu_share);
+    int cs = 1;
+    while (cs < CS && (units * cs < fill || (maxP + cs - 1) / cs > kShortSlice)) cs *= 2;
+    CS = cs;
+  }
   while (CS > 1 && (maxP + CS / 2 - 1) / (CS / 2) <= room &&
          max_active_clusters(CS, smem_for(CS, maxP, p.kp)) < units)
     CS /= 2;
