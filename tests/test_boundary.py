@@ -273,3 +273,38 @@ def test_layers_entry_point_checks_arguments():
                                       ptrs, ptrs, ptrs, 0x10000, both, None, 2, sts,
                                       ev) == S.ERR_UNSUPPORTED
     assert S.workspace_size_layers(bad, [3000], 16, 256, 2) == 0
+
+
+def test_layers_binding_checks_arguments():
+    """compress_layers (Python binding) rejects bad arguments before any CUDA
+    call: counts of outputs, streams and events; CPU or strided tensors;
+    layers of different shapes."""
+    import torch
+
+    def lay(L=3000, W=16, dev="cpu"):
+        q = torch.zeros((1, W, 8, 64), dtype=torch.bfloat16, device=dev)
+        k = torch.zeros((L, 2, 64), dtype=torch.bfloat16, device=dev)
+        return q, k, k.clone()
+
+    def outs(C=256):
+        return (torch.zeros((1, C, 2, 64), dtype=torch.bfloat16),
+                torch.zeros((1, C, 2, 64), dtype=torch.bfloat16),
+                torch.zeros((1, 2, C), dtype=torch.int32))
+
+    ws = torch.zeros(16, dtype=torch.uint8)
+    one = [lay()]
+    with pytest.raises(ValueError):  # no output triple for the layer
+        S.compress_layers(one, [3000], 16, 5, "avg", 256, [], ws, [object()] * 2, [object()] * 3)
+    with pytest.raises(ValueError):  # events: one more than streams
+        S.compress_layers(one, [3000], 16, 5, "avg", 256, [outs()], ws, [object()] * 2,
+                          [object()] * 2)
+    with pytest.raises(ValueError):  # too many streams
+        S.compress_layers(one, [3000], 16, 5, "avg", 256, [outs()], ws,
+                          [object()] * (S.MAX_LAYER_STREAMS + 1),
+                          [object()] * (S.MAX_LAYER_STREAMS + 2))
+    with pytest.raises(ValueError):  # window size disagrees with q_win
+        S.compress_layers(one, [3000], 32, 5, "avg", 256, [outs()], ws, [object()] * 2,
+                          [object()] * 3)
+    with pytest.raises(ValueError):  # CPU tensors
+        S.compress_layers(one, [3000], 16, 5, "avg", 256, [outs()], ws, [object()] * 2,
+                          [object()] * 3)
