@@ -63,6 +63,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-scissorhands", action="store_true")
     ap.add_argument("--no-workloads", action="store_true")
+    ap.add_argument("--no-lse", action="store_true", help="skip the caller's-LSE step")
     ap.add_argument("--layer-streams", type=int, default=4,
                     help="streams snapkv_compress_layers overlaps consecutive layers on (1-4)")
     ap.add_argument("--eager", action="store_true",
@@ -387,6 +388,67 @@ def workload_table(S, torch, dev, peak, names=("1", "2", "3", "5a", "5b"), reps=
     return out
 
 
+def lse_input_step(S, torch, data, outs, wsl, seqlens, cfg, dev, ns, peak, compress_bytes):
+    """The same step with the caller's window LSE (snapkv_compress_layers with
+    lse_wins: pass 2 only, as when the prefill attention kernel returns its
+    row LSE).  The LSE is computed once per layer in plain torch on the device
+    (fp32 logits under the causal mask, torch.logsumexp), outside any timed
+    region; the step is captured in a CUDA graph and replayed."""
+    import math
+
+    W, C, kp, pool = cfg["W"], cfg["C"], cfg["k_pool"], cfg["pool"]
+    H_q, H_kv, d = cfg["H_q"], cfg["H_kv"], cfg["d"]
+    g = H_q // H_kv
+    B = len(seqlens)
+    lses = []
+    for q, k, _ in data:
+        lse = torch.full((B, W, H_q), float("nan"), dtype=torch.float32, device=dev)
+        row0 = 0
+        for b, L in enumerate(seqlens):
+            if L > C:
+                P = L - W
+                kb = k[row0:row0 + L].float()
+                mask = torch.arange(L, device=dev)[None, :] > (P + torch.arange(W, device=dev))[:, None]
+                for h in range(H_kv):
+                    s = torch.einsum("igd,jd->igj", q[b, :, h * g:(h + 1) * g].float(),
+                                     kb[:, h]) / math.sqrt(d)
+                    s.masked_fill_(mask[:, None, :], float("-inf"))
+                    lse[b, :, h * g:(h + 1) * g] = torch.logsumexp(s, dim=-1)
+                    del s
+            row0 += L
+        lses.append(lse)
+    streams = [torch.cuda.Stream() for _ in range(ns)]
+    events = [torch.cuda.Event() for _ in range(ns + 1)]
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        S.compress_layers(data, seqlens, W, kp, pool, C, outs, wsl, streams, events, stream=cap,
+                          lse_wins=lses)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            S.compress_layers(data, seqlens, W, kp, pool, C, outs, wsl, streams, events,
+                              stream=cap, lse_wins=lses)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    a.record()
+    for _ in range(reps):
+        graph.replay()
+    b.record()
+    torch.cuda.synchronize()
+    assert S.get_status(wsl) == S.OK
+    us = 1e3 * a.elapsed_time(b) / reps / len(data)
+    return {"us_per_layer": us, "tokens_per_s": sum(seqlens) / (us / 1e6),
+            "frac_compress": compress_bytes / (us / 1e6) / 1e9 / peak,
+            "note": "the step with the caller's window LSE (pass 2 only), through "
+                    f"snapkv_compress_layers ({ns} layer streams), captured in a CUDA graph; "
+                    "the LSE comes from torch on the device, outside the timed region"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -497,7 +559,7 @@ def main():
     ev_arr = (ctypes.c_void_p * (ns + 1))(*[e.cuda_event for e in layer_events])
 
     def step():
-        rc = lib.snapkv_compress_layers(sh_ref, layers, arrs[0], arrs[1], arrs[2], sl_arr, W, kp,
+        rc = lib.snapkv_compress_layers(sh_ref, layers, arrs[0], arrs[1], arrs[2], None, sl_arr, W, kp,
                                         pool_code, C, arrs[3], arrs[4], arrs[5], wsl.data_ptr(),
                                         wsl.numel(), st, ns, ls_arr, ev_arr)
         if rc:
@@ -612,6 +674,11 @@ def main():
         except Exception:
             traffic = None
 
+    lse_input = None
+    if not args.no_lse and cfg["dtype"] == "bf16":
+        lse_input = lse_input_step(S, torch, data, outs, wsl, seqlens, cfg, dev, ns, peak,
+                                   compress_bytes)
+
     decode = decode_step(S, torch, data, outs, seqlens, cfg, dev, stream, peak)
     sh_decode = None
     if not args.no_scissorhands:
@@ -671,6 +738,7 @@ def main():
             "cpu_baseline": cpu,
             "parity": parity,
             "workloads": workloads,
+            "lse_input": lse_input,
             "e2e": e2e,
             "decode": decode,
             "scissorhands": sh_decode,

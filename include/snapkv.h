@@ -249,16 +249,22 @@ int snapkv_score_offsets(const snapkv_shape *shape, const int32_t *seqlens_host,
  * layer l is enqueued on layer_streams[l % n_streams] with its own part of
  * the workspace, and each layer's score kernel runs on 1/n_streams of the
  * SMs, so that n_streams layers' latency-bound scoring chains (pass 1 ->
- * merge -> pass 2) and their selections run side by side.  Same outputs, bit for bit, as
- * snapkv_compress on each layer.  The call forks the layer streams off
+ * merge -> pass 2) and their selections run side by side.  Same outputs,
+ * bit for bit, as snapkv_compress on each layer.  The call forks the layer
+ * streams off
  * `stream` (events[0]) and joins them back (events[1 .. n_streams]), so work
  * enqueued on `stream` afterwards sees every layer's outputs; it works under
- * stream capture.  Asynchronous; nothing is allocated.
+ * stream capture.  Asynchronous; nothing is allocated.  With lse_win each
+ * layer's outputs equal snapkv_compress_with_lse's instead.
  *
  *   n_layers       >= 1
  *   q_win, k, v    host arrays of n_layers device pointers, each a layer's
  *                  input as in snapkv_compress (all layers share shape,
  *                  seqlens_host, W, kernel_size, pool_type and C)
+ *   lse_win        NULL (the call computes the window rows' LSE, as
+ *                  snapkv_compress), or a host array of n_layers device
+ *                  pointers, each a layer's lse_win as in
+ *                  snapkv_compress_with_lse (pass 2 only)
  *   out_k, out_v, out_idx  host arrays of n_layers device pointers
  *   workspace      device, 256-byte aligned, >= snapkv_workspace_size_layers
  *                  bytes for n_streams (n_streams single-layer workspaces
@@ -285,8 +291,9 @@ size_t snapkv_workspace_size_layers(const snapkv_shape *shape, const int32_t *se
 
 int snapkv_compress_layers(const snapkv_shape *shape, int32_t n_layers,
                            const void *const *q_win, const void *const *k, const void *const *v,
-                           const int32_t *seqlens_host, int32_t W, int32_t kernel_size,
-                           int32_t pool_type, int32_t C, void *const *out_k, void *const *out_v,
+                           const float *const *lse_win, const int32_t *seqlens_host, int32_t W,
+                           int32_t kernel_size, int32_t pool_type, int32_t C,
+                           void *const *out_k, void *const *out_v,
                            int32_t *const *out_idx, void *workspace, size_t workspace_bytes,
                            void *stream, int32_t n_streams, void *const *layer_streams,
                            void *const *events);

@@ -343,8 +343,9 @@ size_t snapkv_workspace_size_layers(const snapkv_shape* shape, const int32_t* se
 
 int snapkv_compress_layers(const snapkv_shape* shape, int32_t n_layers,
                            const void* const* q_win, const void* const* k, const void* const* v,
-                           const int32_t* seqlens_host, int32_t W, int32_t kernel_size,
-                           int32_t pool_type, int32_t C, void* const* out_k, void* const* out_v,
+                           const float* const* lse_win, const int32_t* seqlens_host, int32_t W,
+                           int32_t kernel_size, int32_t pool_type, int32_t C,
+                           void* const* out_k, void* const* out_v,
                            int32_t* const* out_idx, void* workspace, size_t workspace_bytes,
                            void* stream, int32_t n_streams, void* const* layer_streams,
                            void* const* events) {
@@ -355,7 +356,8 @@ int snapkv_compress_layers(const snapkv_shape* shape, int32_t n_layers,
       !layer_streams || !events)
     return SNAPKV_ERR_INVALID_ARG;
   for (int l = 0; l < n_layers; ++l)
-    if (!q_win[l] || !k[l] || !v[l] || !out_k[l] || !out_v[l] || !out_idx[l])
+    if (!q_win[l] || !k[l] || !v[l] || !out_k[l] || !out_v[l] || !out_idx[l] ||
+        (lse_win && (!lse_win[l] || !aligned(lse_win[l], 4))))
       return SNAPKV_ERR_INVALID_ARG;
   for (int i = 0; i < n_streams; ++i) {
     if (!layer_streams[i]) return SNAPKV_ERR_INVALID_ARG;
@@ -387,7 +389,8 @@ int snapkv_compress_layers(const snapkv_shape* shape, int32_t n_layers,
     const int h = l % n_streams;
     first_err = enqueue(shape, q_win[l], k[l], v[l], seqlens_host, W, kernel_size, pool_type, C,
                         out_k[l], out_v[l], out_idx[l], ws + h * part, part, layer_streams[h],
-                        false, nullptr, false, nullptr, nullptr, false, status, share);
+                        false, lse_win ? lse_win[l] : nullptr, false, nullptr, nullptr, false,
+                        status, share);
   }
   // join, whatever happened above: the caller's stream waits for every one
   for (int i = 0; i < n_streams; ++i) {

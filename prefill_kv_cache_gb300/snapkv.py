@@ -127,8 +127,8 @@ def load() -> ctypes.CDLL:
     lib.snapkv_compress_host_layers.restype = ctypes.c_int
     lib.snapkv_workspace_size_layers.argtypes = [shp, vp, i32, i32, i32]
     lib.snapkv_workspace_size_layers.restype = sz
-    lib.snapkv_compress_layers.argtypes = [shp, i32, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp,
-                                           vp, vp, sz, vp, i32, vp, vp]
+    lib.snapkv_compress_layers.argtypes = [shp, i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp,
+                                           vp, vp, vp, sz, vp, i32, vp, vp]
     lib.snapkv_compress_layers.restype = ctypes.c_int
     lib.snapkv_compress_noalloc.argtypes = [shp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp,
                                             vp]
@@ -434,13 +434,15 @@ def workspace_size_layers(shape: snapkv_shape, seqlens, window_size: int,
 
 def compress_layers(layers, seqlens, window_size: int, kernel_size: int, pooling,
                     max_capacity_prompt: int, outs, workspace: torch.Tensor, layer_streams,
-                    events, stream=None) -> None:
+                    events, stream=None, lse_wins=None) -> None:
     """snapkv_compress_layers (include/snapkv.h): layers = [(q_win, k, v)] and
     outs = [(out_k, out_v, out_idx)] of CUDA tensors, one triple per layer;
     layer_streams 1 .. MAX_LAYER_STREAMS torch CUDA streams; workspace a CUDA
     uint8 tensor of workspace_size_layers(..., len(layer_streams)) bytes;
     events len(layer_streams) + 1 torch.cuda.Event.  Asynchronous on
-    `stream` (default: the current stream)."""
+    `stream` (default: the current stream).  lse_wins: None, or one fp32
+    [B, W, H_q] CUDA tensor per layer (the window rows' natural-log LSE, as
+    compress's lse_win), which skips pass 1."""
     n = len(layers)
     ns = len(layer_streams)
     if n < 1 or len(outs) != n or not 1 <= ns <= MAX_LAYER_STREAMS or len(events) != ns + 1:
@@ -467,6 +469,13 @@ def compress_layers(layers, seqlens, window_size: int, kernel_size: int, pooling
         if q.dtype != q0.dtype or k.dtype != q0.dtype or v.dtype != q0.dtype or \
                 ok.dtype != q0.dtype or ov.dtype != q0.dtype or oi.dtype != torch.int32:
             raise ValueError("inputs and out_k / out_v share one dtype; out_idx is int32")
+    if lse_wins is not None:
+        if len(lse_wins) != n:
+            raise ValueError("one lse_win per layer")
+        for t in lse_wins:
+            if not t.is_cuda:
+                raise ValueError("every lse_win must be a CUDA tensor")
+            _check_lse(t, B, W, H_q)
     st = torch.cuda.current_stream() if stream is None else stream
     for e in events:  # torch creates an event's CUDA handle when it is first recorded
         if not e.cuda_event:
@@ -475,9 +484,10 @@ def compress_layers(layers, seqlens, window_size: int, kernel_size: int, pooling
     ptrs = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])
     sts = (ctypes.c_void_p * ns)(*[s.cuda_stream for s in layer_streams])
     ev = (ctypes.c_void_p * (ns + 1))(*[e.cuda_event for e in events])
+    lse_arr = None if lse_wins is None else ptrs(lse_wins)
     rc = load().snapkv_compress_layers(
         ctypes.byref(shape), n, ptrs([l[0] for l in layers]), ptrs([l[1] for l in layers]),
-        ptrs([l[2] for l in layers]), arr, int(window_size), int(kernel_size),
+        ptrs([l[2] for l in layers]), lse_arr, arr, int(window_size), int(kernel_size),
         pool_code(pooling), C, ptrs([o[0] for o in outs]), ptrs([o[1] for o in outs]),
         ptrs([o[2] for o in outs]), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream_handle(st), ns, sts, ev)

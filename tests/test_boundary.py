@@ -246,9 +246,9 @@ def test_layers_entry_point_checks_arguments():
     sts = (ctypes.c_void_p * 2)(0x100, 0x200)
     ev = (ctypes.c_void_p * 3)(fake, fake, fake)
 
-    def call(n, streams=sts, events=ev, ws_bytes=both, p=ptrs, ns=2):
-        return lib.snapkv_compress_layers(ctypes.byref(shape), n, p, p, p, sl, 16, 5, 0, 256, p,
-                                          p, p, 0x10000, ws_bytes, None, ns, streams, events)
+    def call(n, streams=sts, events=ev, ws_bytes=both, p=ptrs, ns=2, lse=None):
+        return lib.snapkv_compress_layers(ctypes.byref(shape), n, p, p, p, lse, sl, 16, 5, 0, 256,
+                                          p, p, p, 0x10000, ws_bytes, None, ns, streams, events)
 
     assert call(0) == S.ERR_INVALID_ARG
     assert call(1, ns=0) == S.ERR_INVALID_ARG
@@ -260,6 +260,10 @@ def test_layers_entry_point_checks_arguments():
     assert call(1, events=(ctypes.c_void_p * 3)(fake, None, fake)) == S.ERR_INVALID_ARG
     assert call(2, p=(ctypes.c_void_p * 2)(fake, None)) == S.ERR_INVALID_ARG
     assert call(2, ws_bytes=both - 256) == S.ERR_WORKSPACE
+    # an LSE array must hold a 4-byte-aligned pointer for every layer
+    assert call(2, lse=(ctypes.c_void_p * 2)(fake, None)) == S.ERR_INVALID_ARG
+    assert call(2, lse=(ctypes.c_void_p * 2)(fake, fake + 2)) == S.ERR_INVALID_ARG
+    assert call(2, lse=(ctypes.c_void_p * 2)(fake, fake), ws_bytes=both - 256) == S.ERR_WORKSPACE
     # three streams want three workspace parts and four events
     three = S.workspace_size_layers(shape, [3000], 16, 256, 3)
     sts3 = (ctypes.c_void_p * 3)(0x100, 0x200, 0x300)
@@ -269,8 +273,8 @@ def test_layers_entry_point_checks_arguments():
     assert call(1, streams=sts3, events=ev4, ws_bytes=three - 256, ns=3) == S.ERR_WORKSPACE
     # unsupported head size, before anything else
     bad = S.make_shape(1, 8, 2, 96, S.BF16)
-    assert lib.snapkv_compress_layers(ctypes.byref(bad), 1, ptrs, ptrs, ptrs, sl, 16, 5, 0, 256,
-                                      ptrs, ptrs, ptrs, 0x10000, both, None, 2, sts,
+    assert lib.snapkv_compress_layers(ctypes.byref(bad), 1, ptrs, ptrs, ptrs, None, sl, 16, 5, 0,
+                                      256, ptrs, ptrs, ptrs, 0x10000, both, None, 2, sts,
                                       ev) == S.ERR_UNSUPPORTED
     assert S.workspace_size_layers(bad, [3000], 16, 256, 2) == 0
 

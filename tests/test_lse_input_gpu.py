@@ -77,3 +77,42 @@ def test_score_with_lse_fills_raw_scores():
     got = parity.unpack_scores(raw.cpu().numpy(), lay.seqlens, lay.H_kv, lay.W, C)
     np.testing.assert_allclose(got[0], np.stack(ora["raw"][0]), rtol=parity.LSE_RTOL,
                                atol=parity.ATOL)
+
+
+@pytest.mark.parametrize("n_streams,graph", [(2, False), (4, True)])
+def test_layers_entry_point_with_lse(n_streams, graph):
+    """snapkv_compress_layers with the caller's LSE per layer: every layer's
+    outputs equal snapkv_compress_with_lse on the same layer, bit for bit,
+    also replayed from a CUDA graph."""
+    C, W, kp = 1024, 32, 7
+    seqlens = [4000, 700, 2600]
+    lays = [synth.make_inputs(60 + l, seqlens, 32, 8, 128, W, "bf16", nspans=4) for l in range(5)]
+    dev = lambda x: torch.from_numpy(x).view(torch.bfloat16).cuda()
+    layers = [(dev(l.q_win), dev(l.k), dev(l.v)) for l in lays]
+    lses = [torch.from_numpy(parity.window_lse(l, C)).cuda() for l in lays]
+    ref = [S.compress_with_lse(q, k, v, lse, seqlens, W, kp, "avg", C)[:3]
+           for (q, k, v), lse in zip(layers, lses)]
+    shape = S.make_shape(len(seqlens), 32, 8, 128, S.BF16)
+    ws = torch.empty(S.workspace_size_layers(shape, seqlens, W, C, n_streams), dtype=torch.uint8,
+                     device="cuda")
+    outs = [tuple(torch.empty_like(x) for x in r) for r in ref]
+    streams = [torch.cuda.Stream() for _ in range(n_streams)]
+    events = [torch.cuda.Event() for _ in range(n_streams + 1)]
+    if graph:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                S.compress_layers(layers, seqlens, W, kp, "avg", C, outs, ws, streams, events,
+                                  stream=cap, lse_wins=lses)
+        for _ in range(2):
+            g.replay()
+    else:
+        S.compress_layers(layers, seqlens, W, kp, "avg", C, outs, ws, streams, events,
+                          lse_wins=lses)
+    torch.cuda.synchronize()
+    assert S.get_status(ws) == S.OK
+    for l, (o, r) in enumerate(zip(outs, ref)):
+        for a, b in zip(o, r):
+            assert torch.equal(a, b), l
