@@ -229,7 +229,7 @@ def test_host_layers_entry_point_matches_device(pinned_v):
 
 @pytest.mark.parametrize("n_layers,n_streams,graph",
                          [(1, 2, False), (5, 2, False), (4, 2, True), (7, 3, False),
-                          (6, 4, True), (3, 1, False)])
+                          (6, 4, True), (3, 1, False), (9, 8, False)])
 def test_layers_entry_point_matches_single_calls(n_layers, n_streams, graph):
     """snapkv_compress_layers runs consecutive layers on n_streams streams,
     each with its own workspace part; every layer's outputs must equal
