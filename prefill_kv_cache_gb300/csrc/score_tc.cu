@@ -15,19 +15,24 @@
 //   pass 2 (S^T = K Q^T, keys on TMEM lanes): each thread sums
 //     exp2(logit * log2e / sqrt(d) - lse2) over all query rows of its key.
 //
-// Kernel shape: persistent, one CTA per SM, 12 warps:
+// Kernel shape: persistent, one CTA per SM (or per SM of the call's share
+// when several calls run side by side):
 //   warp 0  TMA producer (K tiles of 128 keys, Q of the current KV head),
 //   warp 1  MMA issuer (single thread) and TMEM owner (512 columns),
-//   warps 2-3 idle (their warpgroup gives its registers to the consumers),
-//   warps 4-11 two consumer warpgroups; both read every tile's accumulator,
-//     group w its column half, and hand the TMEM buffer back as soon as the
-//     columns are in registers, so the MMA of the tile after next overlaps
-//     their exp2 work.  Pass-2 half sums meet in shared memory.
+//   warp 2  publisher of finished pass-1 pieces and merges (one release each),
+//   warp 3  idle (its warpgroup gives its registers to the consumers),
+//   then NSG consumer super-groups of two warpgroups: super-group s reads
+//     the tiles of TMEM buffer s (NSG = 2 at W*g = 256: alternate tiles; 1 at
+//     128: every tile), warpgroup w of it the column half w; the buffer goes
+//     back to the MMA as soon as the columns are in registers, so the MMA of
+//     the tile after next overlaps their exp2 work.  Pass-2 half sums meet
+//     in the zeroed score array (two addends: order-independent).
 // Work items come from a device-wide queue in the order
 //   P1(0) | P1(1) M(0) | P1(2) M(1) P2(0) | ... | M(G-1) P2(G-2) | P2(G-1)
-// where a group is ~1024 key tiles of whole KV heads, P1 / P2 are pass-1 /
-// pass-2 pieces of 8 tiles and M are merge items.  Pass 2 of a group
-// re-reads K that pass 1 streamed through L2 two groups earlier.  A merge item
+// (small launches: every P1, then every M, then every P2) where a group is
+// ~1024 key tiles of whole KV heads, P1 / P2 are pass-1 / pass-2 pieces of
+// up to 8 tiles and M are merge items.  Pass 2 of a group re-reads K that
+// pass 1 streamed through L2 two groups earlier.  A merge item
 // waits for its group's pass-1 pieces and a pass-2 item for its group's
 // merges; both always sit later in the queue than what they wait for, so
 // the waits cannot form a cycle whatever the number of resident CTAs.
@@ -594,7 +599,7 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
     }
   } else if (warp == 2) {
     // ------------------------------------------------------- helper ---
-    // publishes finished pass-1 items: waits until all 8 consumer warps have
+    // publishes finished pass-1 items: waits until all consumer warps have
     // written an item's statistics, then one device-scope release increment
     // of its group's counter makes them visible to the merge items
     if (lane == 0) {
@@ -846,7 +851,7 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
           if (PER_Q) {
             // every query head keeps its own sum: member m of the group owns
             // the rows r with r % g == m (g divides 8; acc[k] holds the
-            // columns 2k, 2k+1 mod 8); the two groups' halves add up in the
+            // columns 2k, 2k+1 mod 8); the two warpgroups' halves add up in the
             // zeroed score array (two addends onto zero: order-independent)
             float am[8];
 #pragma unroll
@@ -862,7 +867,7 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
               }
             }
           } else if (key < S.P) {
-            // the two groups' halves meet in the zeroed score array (two
+            // the two warpgroups' halves meet in the zeroed score array (two
             // addends onto zero: the result does not depend on their order)
             atomicAdd(raw_out + key, sum4(acc) * inv_g);
           }
@@ -881,8 +886,9 @@ score_tc_kernel(const __grid_constant__ Plan p, const __grid_constant__ TcPlan t
           for (int m = 0; m < rows; ++m)
             for (int k = k_lo + ct; k < k_hi; k += kConsumerThreads) z[(size_t)m * S.P + k] = 0.f;
         }
-        // publish this row's statistics for the piece (slot wg with one row
-        // block, where the two groups hold halves of the keys); the
+        // publish this row's statistics for the piece (slot sg with two row
+        // blocks; 2 sg + wg with one, where the two warpgroups hold halves of
+        // the keys); the
         // device-scope release that publishes them takes a while (it waits
         // for this warp's writes to land): the helper warp does it
         const size_t piece = (size_t)S.piece0 + (size_t)h * S.chunks + e.piece;
